@@ -1,0 +1,460 @@
+"""Benchmark of the row-normalisation hot path on GB300.
+
+One step = one forward and one backward (trainable: dW / dB computed) of
+RMSNorm, LayerNorm and FusedAddRMSNorm on bf16 activations of M x N
+(default 8192 x 8192), i.e. every row kernel of the path plus the dW / dB
+column reductions, each operation on its own seeded synthetic tensors.
+The operations run in the order rms_fwd, ln_fwd, fadd_fwd, rms_bwd, ln_bwd,
+fadd_bwd so that no two consecutive operations touch the same tensor, and
+L2 is flushed (a write larger than twice the L2) before every step.
+
+Reported (one JSON line on rank 0):
+  value        algorithmic HBM bytes of the step / device time of the step
+               (CUDA events on the launching stream, L2 flush excluded), GB/s,
+               summed over ranks (each rank runs its own replica);
+  roofline     the dominant operation (largest share of the step): its
+               algorithmic bytes per call / its mean event-timed duration,
+               against the measured HBM copy bandwidth;
+  per_op       the same for every operation, trainable and frozen;
+  e2e          the same metric with host buffers: pinned host -> device copies
+               of every input and device -> host copies of every output inside
+               the timed region, through the same C-ABI calls;
+  cpu_baseline the FP64 CPU oracle on a bounded row sample of the same
+               workload, on this host's cores (a reported baseline).
+
+--impl reference times that oracle alone (the pages give no runnable
+reference implementation), on the same metric and workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic_inputs as si  # noqa: E402
+
+METRIC = ("HBM GB/s (% of GB300 peak) & µs/call, bf16 RMSNorm/LayerNorm fwd+bwd at 8192×8192")
+OPS = ["rms_fwd", "ln_fwd", "fadd_fwd", "rms_bwd", "ln_bwd", "fadd_bwd"]
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (reads of x, dy, residual, dh_out, w, b, rstd, mean plus
+# writes of y, h, dx, rstd, mean, dW, dB)
+# ---------------------------------------------------------------------------
+def op_bytes(op, M, N, s=2, sw=2, trainable=True):
+    MN = M * N
+    if op == "rms_fwd":
+        return 2 * MN * s + N * sw + 4 * M
+    if op == "rms_bwd":
+        return 3 * MN * s + N * sw + 4 * M + (N * sw if trainable else 0)
+    if op == "ln_fwd":
+        return 2 * MN * s + 2 * N * sw + 8 * M
+    if op == "ln_bwd":
+        return 3 * MN * s + N * sw + 8 * M + (2 * N * sw if trainable else 0)
+    if op == "fadd_fwd":
+        return 4 * MN * s + N * sw + 4 * M
+    if op == "fadd_bwd":
+        return 4 * MN * s + N * sw + 4 * M + (N * sw if trainable else 0)
+    raise ValueError(op)
+
+
+def launches_per_op(op, trainable=True):
+    return 2 if (op.endswith("_bwd") and trainable) else 1
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        v = d.get("hbm_gbs") or d.get("hbm_GBps") or d.get("hbm")
+        if isinstance(v, dict):
+            v = v.get("value")
+        if v:
+            return float(v), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+def host_inputs(M, N, seed=0):
+    """CPU tensors of every operation (distinct seeds per operation)."""
+    rms = si.norm_case(M, N, seed=seed, dtype="bfloat16", with_bias=False)
+    ln = si.norm_case(M, N, seed=seed + 1, dtype="bfloat16")
+    fa = si.norm_case(M, N, seed=seed + 2, dtype="bfloat16", with_bias=False, fused_add=True)
+    return {"rms": rms, "ln": ln, "fadd": fa}
+
+
+class Workload:
+    """Device tensors of one step; `run(op)` issues one operation."""
+
+    def __init__(self, g, host, M, N, dev="cuda"):
+        self.g, self.M, self.N = g, M, N
+        bf = torch.bfloat16
+        e = lambda: torch.empty(M, N, dtype=bf, device=dev)  # noqa: E731
+        f32 = lambda n: torch.empty(n, dtype=torch.float32, device=dev)  # noqa: E731
+        self.t = {}
+        for k, case in host.items():
+            for name, v in case.items():
+                self.t[f"{k}.{name}"] = v.to(dev)
+        for k in ("rms", "ln", "fadd"):
+            self.t[f"{k}.y"] = e()
+            self.t[f"{k}.dx"] = e()
+            self.t[f"{k}.rstd"] = f32(M)
+            self.t[f"{k}.dw"] = torch.empty(N, dtype=bf, device=dev)
+        self.t["ln.mean"] = f32(M)
+        self.t["ln.db"] = torch.empty(N, dtype=bf, device=dev)
+        self.t["fadd.h"] = e()
+        nb = max(g.norm_bwd_workspace_bytes(M, N, True, True), 16)
+        self.ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+
+    def run(self, op, trainable=True, stream=None):
+        g, t = self.g, self.t
+        ws = self.ws if trainable else None
+        if op == "rms_fwd":
+            g.norm_rms_fwd(t["rms.x"], t["rms.w"], t["rms.y"], t["rms.rstd"], 0.0, 1e-6, stream)
+        elif op == "ln_fwd":
+            g.norm_ln_fwd(t["ln.x"], t["ln.w"], t["ln.b"], t["ln.y"], t["ln.mean"], t["ln.rstd"], 0.0, 1e-6,
+                          stream)
+        elif op == "fadd_fwd":
+            g.norm_fused_add_rms_fwd(t["fadd.x"], t["fadd.residual"], t["fadd.w"], t["fadd.y"], t["fadd.h"],
+                                     t["fadd.rstd"], 0.0, 1e-6, stream)
+        elif op == "rms_bwd":
+            g.norm_rms_bwd(t["rms.dy"], t["rms.x"], t["rms.w"], t["rms.rstd"], t["rms.dx"],
+                           t["rms.dw"] if trainable else None, ws, 0.0, 1e-6, stream)
+        elif op == "ln_bwd":
+            g.norm_ln_bwd(t["ln.dy"], t["ln.x"], t["ln.w"], t["ln.mean"], t["ln.rstd"], t["ln.dx"],
+                          t["ln.dw"] if trainable else None, t["ln.db"] if trainable else None, ws, 0.0, 1e-6,
+                          stream)
+        elif op == "fadd_bwd":
+            g.norm_fused_add_rms_bwd(t["fadd.dy"], t["fadd.dh_out"], t["fadd.h"], t["fadd.w"], t["fadd.rstd"],
+                                     t["fadd.dx"], t["fadd.dw"] if trainable else None, ws, 0.0, 1e-6, stream)
+        else:
+            raise ValueError(op)
+
+    # tensors a host-buffer user supplies / reads back, per operation
+    IN = {"rms_fwd": ["rms.x", "rms.w"], "ln_fwd": ["ln.x", "ln.w", "ln.b"],
+          "fadd_fwd": ["fadd.x", "fadd.residual", "fadd.w"],
+          "rms_bwd": ["rms.dy"], "ln_bwd": ["ln.dy"], "fadd_bwd": ["fadd.dy", "fadd.dh_out"]}
+    OUT = {"rms_fwd": ["rms.y"], "ln_fwd": ["ln.y"], "fadd_fwd": ["fadd.y", "fadd.h"],
+           "rms_bwd": ["rms.dx", "rms.dw"], "ln_bwd": ["ln.dx", "ln.dw", "ln.db"],
+           "fadd_bwd": ["fadd.dx", "fadd.dw"]}
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax.append(float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline
+# ---------------------------------------------------------------------------
+def oracle_step(host, rows):
+    """Run the oracle on the first `rows` rows of every operation's inputs.
+    Returns (seconds, algorithmic bytes of that sample)."""
+    import oracle
+    f = lambda t: t[:rows].double().numpy()  # noqa: E731
+    w = {k: host[k]["w"].double().numpy() for k in host}
+    rms, ln, fa = host["rms"], host["ln"], host["fadd"]
+    a = dict(rx=f(rms["x"]), rdy=f(rms["dy"]), lx=f(ln["x"]), ldy=f(ln["dy"]), lb=ln["b"].double().numpy(),
+             fx=f(fa["x"]), fr=f(fa["residual"]), fdy=f(fa["dy"]), fdh=f(fa["dh_out"]))
+    N = a["rx"].shape[1]
+    t0 = time.perf_counter()
+    oracle.rms_fwd(a["rx"], w["rms"], 0.0, 1e-6)
+    oracle.ln_fwd(a["lx"], w["ln"], a["lb"], 0.0, 1e-6)
+    _, h, _ = oracle.fused_add_rms_fwd(a["fx"], a["fr"], w["fadd"], 0.0, 1e-6)
+    oracle.rms_bwd(a["rx"], a["rdy"], w["rms"], 0.0, 1e-6)
+    oracle.ln_bwd(a["lx"], a["ldy"], w["ln"], 0.0, 1e-6)
+    oracle.fused_add_rms_bwd(h, a["fdy"], w["fadd"], a["fdh"], 0.0, 1e-6)
+    dt = time.perf_counter() - t0
+    return dt, sum(op_bytes(op, rows, N) for op in OPS)
+
+
+def cpu_baseline(host, target_s=10.0):
+    import oracle
+    oracle.build()
+    M = host["rms"]["x"].shape[0]
+    rows = min(M, 16)
+    dt, _ = oracle_step(host, rows)
+    rows = int(min(M, max(16, rows * target_s / max(dt, 1e-3))))
+    dt, nbytes = oracle_step(host, rows)
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows} rows of each of the 6 operations at N={host['rms']['x'].shape[1]} "
+                      f"(single-threaded FP64 C oracle, {dt:.1f} s)"}
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    M, N = args.M, args.N
+    host = host_inputs(M, N, seed=0)
+    import oracle
+    oracle.build()
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_step(host, rows)
+    times, nbytes = [], 0
+    for _ in range(args.steps):
+        dt, nbytes = oracle_step(host, rows)
+        times.append(dt)
+    total = sum(times)
+    value = nbytes * args.steps / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"bf16 {M}x{N} RMSNorm+LayerNorm+FusedAddRMSNorm fwd+bwd (trainable)",
+                   "M": M, "N": N, "sample_rows": rows},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{rows} rows of each of the 6 operations per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--M", type=int, default=8192)
+    ap.add_argument("--N", type=int, default=8192)
+    ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import row_normalization_rmsnorm_gb300 as g
+
+    M, N = args.M, args.N
+    host = host_inputs(M, N, seed=rank)
+    wl = Workload(g, host, M, N)
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
+
+    def step(events=None):
+        flush.zero_()
+        if events is not None:
+            events[0].record(stream)
+        for i, op in enumerate(OPS):
+            wl.run(op, True, stream)
+            if events is not None:
+                events[i + 1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(OPS) + 1)] for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for k in range(args.steps):
+            step(evs[k])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    op_ms = {op: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)] for i, op in enumerate(OPS)}
+    step_ms = [evs[k][0].elapsed_time(evs[k][-1]) for k in range(args.steps)]
+    ms_step = sum(step_ms) / len(step_ms)
+    if ws > 1:
+        t = torch.tensor([ms_step], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    step_bytes = sum(op_bytes(op, M, N) for op in OPS)
+    value = step_bytes * ws / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+
+    # per-operation figures, trainable (inside the timed steps) and frozen
+    per_op = {}
+    for op in OPS:
+        us = 1e3 * statistics.mean(op_ms[op])
+        b = op_bytes(op, M, N)
+        per_op[op] = {"us": us, "GBps": b / us / 1e3, "frac": b / us / 1e3 / peak, "bytes": b}
+    for op in ("rms_bwd", "ln_bwd", "fadd_bwd"):
+        ts = []
+        for _ in range(max(5, args.steps // 2)):
+            flush.zero_()
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            wl.run(op, False, stream)
+            b_.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b_))
+        us = 1e3 * statistics.mean(ts)
+        b = op_bytes(op, M, N, trainable=False)
+        per_op[op + "_frozen"] = {"us": us, "GBps": b / us / 1e3, "frac": b / us / 1e3 / peak, "bytes": b}
+
+    dom = max(OPS, key=lambda op: per_op[op]["us"])
+    prof = load_profile_traffic(dom, M, N)
+    roofline = {"bound": "hbm", "kernel": f"{dom} (row kernel"
+                + (" + dW/dB column reduce)" if dom.endswith("_bwd") else ")"),
+                "achieved": per_op[dom]["GBps"], "peak": peak, "unit": "GB/s",
+                "frac": per_op[dom]["GBps"] / peak, "traffic": prof, "peak_kind": peak_kind,
+                "algorithmic_bytes_per_call": per_op[dom]["bytes"]}
+
+    # end to end: host buffers, copies inside the timed region
+    e2e = run_e2e(wl, stream, args.e2e_steps, M, N)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(host)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"bf16 {M}x{N} RMSNorm+LayerNorm+FusedAddRMSNorm fwd+bwd (trainable)",
+                       "M": M, "N": N, "ops": OPS,
+                       "l2": "flushed before every step (zero-fill of 2x L2); every tensor > L2",
+                       "timing": "CUDA events on the launching stream; flush excluded",
+                       "wall_s_timed_region": wall, "parallelism": f"replicas x{ws}"},
+            "roofline": roofline,
+            "per_op": per_op,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "gpu_launches": args.steps * sum(launches_per_op(op) for op in OPS),
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def load_profile_traffic(op, M, N):
+    """dram bytes per call of the operation's kernels from the committed ncu
+    summary, if one exists for this exact workload; else None."""
+    path = os.path.join(ROOT, "profiles", f"ncu_traffic_{M}x{N}.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get(op)
+    except (OSError, ValueError):
+        return None
+
+
+def run_e2e(wl, stream, steps, M, N):
+    """Same metric through the same calls, from pinned host buffers."""
+    host_in = {k: torch.empty_like(wl.t[k], device="cpu").pin_memory()
+               for op in OPS for k in Workload.IN[op]}
+    for k, v in host_in.items():
+        v.copy_(wl.t[k])
+    host_out = {k: torch.empty_like(wl.t[k], device="cpu").pin_memory()
+                for op in OPS for k in Workload.OUT[op]}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def one():
+        for op in OPS:
+            for k in Workload.IN[op]:
+                wl.t[k].copy_(host_in[k], non_blocking=True)
+            wl.run(op, True, stream)
+            for k in Workload.OUT[op]:
+                host_out[k].copy_(wl.t[k], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    step_bytes = sum(op_bytes(op, M, N) for op in OPS)
+    return {"value": step_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,226 @@
+/*
+ * gb300norm.h -- C ABI of the GB300 (sm_103a) row-normalisation library
+ * libgb300norm.so: RMSNorm, LayerNorm and FusedAddRMSNorm, forward and
+ * backward, over an M x N activation matrix.
+ *
+ * Operations (per row i of M, columns j < N; W'_j = float(w_j) + offset is
+ * formed in FP32 inside the kernels, never pre-added in the weight's storage
+ * type -- "fix(cutedsl): fuse Gemma RMSNorm weight offset in FP32", Summary):
+ *
+ *   RMSNorm     rstd = 1/sqrt(mean_j(x_j^2) + eps);  y_j = x_j*rstd*W'_j
+ *   LayerNorm   mean = mean_j(x_j); rstd = 1/sqrt(mean_j((x_j-mean)^2) + eps)
+ *               y_j = (x_j-mean)*rstd*W'_j + b_j
+ *   FusedAdd    h_j = x_j + residual_j;  y = RMSNorm(h);  h is also an output
+ *
+ * Backward passes compute dx always and the column-reduced dW (and dB) only
+ * when the caller passes a non-NULL dw (db) pointer: a NULL pointer selects a
+ * kernel instantiation with every weight-gradient instruction, partial buffer
+ * and reduction compiled out ("perf(norm): skip dW/dB calculation when
+ * parameters are frozen", Motivation and Key Changes).
+ *
+ * Common conventions
+ *   - Every tensor pointer is a DEVICE pointer on the current CUDA device,
+ *     owned by the caller.  The library never allocates or frees memory and
+ *     never synchronises the host; every call only enqueues kernels on
+ *     `stream` (NULL = the legacy default stream) and returns.
+ *   - 2-D tensors are row-major with a per-tensor row stride in ELEMENTS
+ *     (stride >= N); row i of x starts at x + i*x_stride.
+ *   - dtype codes: NORM_F32, NORM_F16, NORM_BF16.  Activations (x, y,
+ *     residual, h, dy, dx, dh_out) have type `dtype`; weights and bias have
+ *     type `w_dtype`.  Supported (dtype, w_dtype): (F32,F32), (F16,F16),
+ *     (BF16,BF16), (BF16,F32), (F16,F32).  All arithmetic is FP32.
+ *   - mean / rstd are FP32 arrays of length M (contiguous).
+ *   - dW / dB outputs are length-N contiguous arrays of type `dw_dtype`, which
+ *     must be NORM_F32 or equal to w_dtype.  They are reduced over all rows in
+ *     a fixed order (bit-reproducible run to run).
+ *   - A backward with dW or dB needs a caller-provided device workspace of at
+ *     least the size norm_bwd_workspace_bytes() reports (16-byte aligned); a
+ *     frozen backward (dw = db = NULL) needs none (workspace may be NULL).
+ *   - Aliasing: y may be x, dx may be dy, h_out may be x or residual, and the
+ *     fused-add dx may be dy or dh_out, each only with equal row strides.  Any
+ *     other overlap between an output and any other argument is undefined.
+ *   - M == 0 is a successful no-op (dW/dB, if requested, are set to zero).
+ *   - Return value: NORM_OK or an error code.  Argument errors are detected on
+ *     the host before anything is enqueued.  NORM_ERR_CUDA reports a CUDA
+ *     runtime error returned while querying the device or launching.
+ *     Faults that happen later on the device surface at the caller's next
+ *     synchronisation, as with any CUDA kernel.
+ */
+#ifndef GB300NORM_H
+#define GB300NORM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define GB300NORM_API __attribute__((visibility("default")))
+#else
+#define GB300NORM_API
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *gb300norm_stream_t;
+
+/* Element type codes. */
+enum { NORM_F32 = 0, NORM_F16 = 1, NORM_BF16 = 2 };
+
+/* Status codes. */
+enum {
+    NORM_OK = 0,
+    NORM_ERR_NULL = 1,      /* a required pointer is NULL                      */
+    NORM_ERR_SHAPE = 2,     /* M < 0, N <= 0 or N > 2^31 - 1                    */
+    NORM_ERR_STRIDE = 3,    /* a row stride < N                                 */
+    NORM_ERR_DTYPE = 4,     /* unsupported dtype / w_dtype / dw_dtype           */
+    NORM_ERR_WORKSPACE = 5, /* workspace NULL, too small or not 16-B aligned    */
+    NORM_ERR_ALIGN = 6,     /* a pointer is not aligned to its element size     */
+    NORM_ERR_VALUE = 7,     /* eps < 0, or eps / offset not finite              */
+    NORM_ERR_ALIAS = 8,     /* an output overlaps an input in a way not allowed */
+    NORM_ERR_CUDA = 9,      /* CUDA runtime error while querying or launching   */
+    NORM_ERR_ARG = 10       /* inconsistent optional arguments (see each call)  */
+};
+
+/* Human-readable name of a status code (static string, never NULL). */
+GB300NORM_API const char *norm_status_str(int status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+GB300NORM_API int norm_version(void);
+
+/*
+ * Workspace a backward call needs for its dW / dB partial sums, in bytes, for
+ * the current device: *bytes = 0 when has_dw == has_db == 0 (frozen).  The
+ * same (M, N, has_dw, has_db) on the same device always gives the same size,
+ * and one workspace of that size serves norm_rms_bwd, norm_ln_bwd and
+ * norm_fused_add_rms_bwd.  Returns NORM_ERR_NULL if bytes is NULL,
+ * NORM_ERR_SHAPE for a bad M / N, NORM_ERR_CUDA if the device cannot be
+ * queried.
+ */
+GB300NORM_API int norm_bwd_workspace_bytes(int64_t M, int64_t N, int has_dw, int has_db,
+                             size_t *bytes);
+
+/*
+ * RMSNorm forward ("fix(cutedsl): fuse Gemma RMSNorm weight offset in FP32",
+ * Summary; offset = 1 gives the Gemma form y = x*rstd*(1 + w)).
+ *   x    [M, x_stride]  in    dtype
+ *   w    [N]            in    w_dtype
+ *   y    [M, y_stride]  out   dtype
+ *   rstd [M]            out   FP32, may be NULL (inference)
+ */
+GB300NORM_API int norm_rms_fwd(const void *x, int64_t x_stride, const void *w,
+                 void *y, int64_t y_stride, float *rstd,
+                 int64_t M, int64_t N, float offset, float eps,
+                 int dtype, int w_dtype, gb300norm_stream_t stream);
+
+/*
+ * RMSNorm backward ("perf(norm): skip dW/dB calculation when parameters are
+ * frozen", Key Changes, rms_norm):
+ *   xhat = x*rstd, g = dy*W', c = mean_j(g_j*xhat_j),
+ *   dx = rstd*(g - xhat*c),  dw = sum over rows of dy*xhat.
+ *   dy   [M, dy_stride] in;  x [M, x_stride] in;  w [N] in
+ *   rstd [M] in, FP32 as saved by the forward; NULL = recompute from x, eps
+ *   dx   [M, dx_stride] out (may alias dy)
+ *   dw   [N] out of type dw_dtype, NULL = frozen weight (no dW work at all)
+ *   workspace / workspace_bytes: see norm_bwd_workspace_bytes (unused if
+ *   dw is NULL)
+ */
+GB300NORM_API int norm_rms_bwd(const void *dy, int64_t dy_stride,
+                 const void *x, int64_t x_stride,
+                 const void *w, const float *rstd,
+                 void *dx, int64_t dx_stride,
+                 void *dw, int dw_dtype,
+                 void *workspace, size_t workspace_bytes,
+                 int64_t M, int64_t N, float offset, float eps,
+                 int dtype, int w_dtype, gb300norm_stream_t stream);
+
+/*
+ * LayerNorm forward ("perf(norm): skip dW/dB ...", Key Changes, layer_norm),
+ * biased variance, two passes over the row held on chip.
+ *   b may be NULL (no bias); mean and rstd may each be NULL.
+ */
+GB300NORM_API int norm_ln_fwd(const void *x, int64_t x_stride,
+                const void *w, const void *b,
+                void *y, int64_t y_stride,
+                float *mean, float *rstd,
+                int64_t M, int64_t N, float offset, float eps,
+                int dtype, int w_dtype, gb300norm_stream_t stream);
+
+/*
+ * LayerNorm backward ("perf(norm): skip dW/dB ...", Key Changes, layer_norm;
+ * dW and dB are independent):
+ *   xhat = (x-mean)*rstd, g = dy*W',
+ *   dx = rstd*(g - mean_j(g_j) - xhat*mean_j(g_j*xhat_j)),
+ *   dw = sum over rows of dy*xhat, db = sum over rows of dy.
+ *   mean and rstd must both be given or both be NULL (NULL = recompute from
+ *   x and eps; one NULL and one not gives NORM_ERR_ARG).
+ *   dw, db: NULL = frozen; both use dw_dtype.
+ */
+GB300NORM_API int norm_ln_bwd(const void *dy, int64_t dy_stride,
+                const void *x, int64_t x_stride,
+                const void *w, const float *mean, const float *rstd,
+                void *dx, int64_t dx_stride,
+                void *dw, void *db, int dw_dtype,
+                void *workspace, size_t workspace_bytes,
+                int64_t M, int64_t N, float offset, float eps,
+                int dtype, int w_dtype, gb300norm_stream_t stream);
+
+/*
+ * FusedAddRMSNorm forward ("perf(norm): skip dW/dB ...", Key Changes,
+ * fused_add_rms_norm; "fix(cutedsl): ...", Summary):
+ *   h = x + residual in FP32;  h_out = h rounded to dtype;
+ *   y = RMSNorm of the FP32 h with scale W';  rstd saved (may be NULL).
+ *   h_out may alias x or residual (vLLM-style in-place residual update).
+ */
+GB300NORM_API int norm_fused_add_rms_fwd(const void *x, int64_t x_stride,
+                           const void *residual, int64_t residual_stride,
+                           const void *w,
+                           void *y, int64_t y_stride,
+                           void *h_out, int64_t h_stride,
+                           float *rstd,
+                           int64_t M, int64_t N, float offset, float eps,
+                           int dtype, int w_dtype, gb300norm_stream_t stream);
+
+/*
+ * FusedAddRMSNorm backward, at the saved (rounded) h rows ("fix(cutedsl):
+ * ...", PyTorch accuracy comparison: the backward uses the rounded saved
+ * residual):
+ *   dx = RMSNorm-backward(h, dy) + dh_out.  dx is both d(x) and d(residual).
+ *   dh_out: gradient arriving on the h output, NULL = zero.
+ *   rstd: as saved by the forward, NULL = recompute from h and eps.
+ *   dw: NULL = frozen.
+ */
+GB300NORM_API int norm_fused_add_rms_bwd(const void *dy, int64_t dy_stride,
+                           const void *dh_out, int64_t dh_stride,
+                           const void *h, int64_t h_stride,
+                           const void *w, const float *rstd,
+                           void *dx, int64_t dx_stride,
+                           void *dw, int dw_dtype,
+                           void *workspace, size_t workspace_bytes,
+                           int64_t M, int64_t N, float offset, float eps,
+                           int dtype, int w_dtype, gb300norm_stream_t stream);
+
+/*
+ * Device-side status word shared by all kernels of this library on the
+ * current device: 0 when no kernel has reported a problem.  A kernel whose
+ * bounded wait for an asynchronous row copy runs out sets it (non-zero) and
+ * returns early instead of hanging.  This call synchronises the device; with
+ * reset != 0 the word is cleared afterwards.  Returns NORM_OK or
+ * NORM_ERR_CUDA; *value receives the word.
+ */
+GB300NORM_API int norm_device_status(int reset, int *value);
+
+/*
+ * Test hook: mode 0 (default) lets each call pick its kernel family from the
+ * arguments; mode 2 makes every subsequent call in the process use the
+ * general (any alignment) row kernels, so tests can compare both families
+ * on the same inputs.  Returns NORM_OK or NORM_ERR_ARG.
+ */
+GB300NORM_API int norm_debug_set_path(int mode);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300NORM_H */

@@ -1,0 +1,57 @@
+// colreduce.cu -- stage 2 of the dW / dB column reduction.
+//
+// The row kernels leave one FP32 partial row per CTA ([G][N]).  Each CTA of
+// this kernel owns 32 adjacent columns: its 8 warps sum interleaved subsets of
+// the partial rows (warp k takes rows k, k+8, ...), coalesced 128-byte row
+// segments, and warp 0 adds the 8 subtotals in order.  The order of every
+// addition is fixed by (G, N), so dW / dB are bit-identical from run to run.
+// With G = 0 (no rows) the outputs are set to zero.
+#include "launch.h"
+
+namespace gb300norm {
+
+template <class TO>
+__global__ void __launch_bounds__(256) colreduce_kernel(const float* __restrict__ ws0, TO* __restrict__ out0,
+                                                        const float* __restrict__ ws1, TO* __restrict__ out1,
+                                                        int G, int N) {
+  const float* ws = blockIdx.y ? ws1 : ws0;
+  TO* out = blockIdx.y ? out1 : out0;
+  const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
+  const int col = blockIdx.x * 32 + lane;
+  __shared__ float part[8][33];
+  float acc = 0.f;
+  if (col < N) {
+    for (int g = grp; g < G; g += 8) acc = fadd(acc, ws[(int64_t)g * N + col]);
+  }
+  part[grp][lane] = acc;
+  __syncthreads();
+  if (grp == 0 && col < N) {
+    float s = part[0][lane];
+#pragma unroll
+    for (int k = 1; k < 8; ++k) s = fadd(s, part[k][lane]);
+    out[col] = from_f<TO>(s);
+  }
+}
+
+template <class TO>
+static int launch_cr(const float* a, void* da, const float* b, void* db, int G, int N, cudaStream_t st) {
+  dim3 grid((unsigned)((N + 31) / 32), db ? 2u : 1u);
+  colreduce_kernel<TO><<<grid, 256, 0, st>>>(a, static_cast<TO*>(da), b, static_cast<TO*>(db), G, N);
+  return cudaGetLastError() == cudaSuccess ? NORM_OK : NORM_ERR_CUDA;
+}
+
+int launch_colreduce(const float* ws_dw, void* dw, const float* ws_db, void* db, int G, int N, int out_dtype,
+                     cudaStream_t st) {
+  // The kernel takes one (partial, output) pair per blockIdx.y; when only dB
+  // is wanted it goes in the first slot.
+  if (!dw) { ws_dw = ws_db; dw = db; ws_db = nullptr; db = nullptr; }
+  if (!dw) return NORM_OK;
+  switch (out_dtype) {
+    case NORM_F32: return launch_cr<float>(ws_dw, dw, ws_db, db, G, N, st);
+    case NORM_F16: return launch_cr<__half>(ws_dw, dw, ws_db, db, G, N, st);
+    case NORM_BF16: return launch_cr<__nv_bfloat16>(ws_dw, dw, ws_db, db, G, N, st);
+    default: return NORM_ERR_DTYPE;
+  }
+}
+
+}  // namespace gb300norm

@@ -1,0 +1,201 @@
+// common.cuh -- shared device helpers of the row-normalisation kernels:
+// element types, FP32 arithmetic with fixed rounding, warp/CTA reductions and
+// the PTX wrappers for mbarriers and bulk (TMA-engine) copies.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gb300norm {
+
+// ---------------------------------------------------------------------------
+// Operation kinds and launch parameters
+// ---------------------------------------------------------------------------
+enum OpKind : int { RMS_FWD = 0, RMS_BWD = 1, LN_FWD = 2, LN_BWD = 3, FADD_FWD = 4, FADD_BWD = 5 };
+
+// One struct for every kernel; unused fields are null / zero.
+struct RowParams {
+  // streamed row inputs (element strides)
+  const void* in0;  int64_t s_in0;   // x (h for FADD_BWD)
+  const void* in1;  int64_t s_in1;   // dy (backward) or residual (FADD_FWD)
+  const void* in2;  int64_t s_in2;   // dh_out (FADD_BWD), nullable
+  // row outputs
+  void* out0;       int64_t s_out0;  // y (forward) or dx (backward)
+  void* out1;       int64_t s_out1;  // h_out (FADD_FWD)
+  // per-column parameters
+  const void* w;
+  const void* b;                     // LayerNorm bias, nullable
+  // per-row statistics
+  float* mean_out;  float* rstd_out;       // forward, nullable
+  const float* mean_in; const float* rstd_in;  // backward, nullable = recompute
+  // dW / dB partial rows, [gridDim.x][N] FP32
+  float* ws_dw;     float* ws_db;
+  int64_t M;
+  int N;
+  float offset;
+  float eps;
+  int* status;      // device status word (bounded waits that ran out)
+};
+
+// ---------------------------------------------------------------------------
+// Element types
+// ---------------------------------------------------------------------------
+template <class T> struct Elem;
+template <> struct Elem<float> {
+  static __device__ __forceinline__ float to_f(float v) { return v; }
+  static __device__ __forceinline__ float from_f(float v) { return v; }
+};
+template <> struct Elem<__half> {
+  static __device__ __forceinline__ float to_f(__half v) { return __half2float(v); }
+  static __device__ __forceinline__ __half from_f(float v) { return __float2half_rn(v); }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+};
+
+template <class T> __device__ __forceinline__ float to_f(T v) { return Elem<T>::to_f(v); }
+template <class T> __device__ __forceinline__ T from_f(float v) { return Elem<T>::from_f(v); }
+
+// 16 bytes of T as an array; VEC elements.
+template <class T> struct Vec16 {
+  static constexpr int VEC = 16 / (int)sizeof(T);
+  union { uint4 u; T e[16 / sizeof(T)]; };
+};
+
+// ---------------------------------------------------------------------------
+// FP32 arithmetic with explicit rounding.  Every value a kernel writes is
+// computed through these, so the compiler cannot contract or reorder them
+// differently between the trainable and the frozen instantiation of a
+// kernel: the input gradient is bit-identical in both.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float fmul(float a, float b) { return __fmul_rn(a, b); }
+__device__ __forceinline__ float fadd(float a, float b) { return __fadd_rn(a, b); }
+__device__ __forceinline__ float fsub(float a, float b) { return __fsub_rn(a, b); }
+__device__ __forceinline__ float ffma(float a, float b, float c) { return __fmaf_rn(a, b, c); }
+
+// ---------------------------------------------------------------------------
+// Reductions.  Butterfly shuffles give every lane the same sum (each step adds
+// the same two operands on both partners); warps are combined in a fixed
+// order.  `red` holds two banks of [32 warps][NV] floats used alternately so
+// that consecutive reductions need only one barrier each.
+// ---------------------------------------------------------------------------
+template <int NV>
+__device__ __forceinline__ void warp_sum(float (&v)[NV]) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = fadd(v[i], __shfl_xor_sync(0xffffffffu, v[i], o));
+}
+
+template <int NV>
+__device__ __forceinline__ void block_sum(float (&v)[NV], float* red, int& bank) {
+  warp_sum<NV>(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
+  float* r = red + bank * 32 * NV;
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) r[warp * NV + i] = v[i];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < NV; ++i) v[i] = r[i];
+  for (int k = 1; k < nw; ++k) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = fadd(v[i], r[k * NV + i]);
+  }
+  bank ^= 1;
+}
+
+// 1/sqrt(m + eps).
+__device__ __forceinline__ float inv_rms(float m, float eps) { return rsqrtf(fadd(m, eps)); }
+
+// ---------------------------------------------------------------------------
+// mbarrier and bulk-copy PTX (sm_90+ instructions, used on sm_103a)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Upper bound of any single wait for a row copy.  A copy of at most a few
+// hundred KB lands in microseconds; the bound only ends a wait that would
+// otherwise never finish.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+
+// Wait until the phase with the given parity of `bar` has completed.
+// Returns false (and leaves the barrier untouched) if kWaitLimitNs passes.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Bulk copy global -> shared through the TMA engine, completing `bytes` of
+// transaction count on `bar`.  dst, src 16-byte aligned; bytes % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// 16-byte global store with the streaming (evict-first) hint.
+__device__ __forceinline__ void st_global_cs16(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Status bits written to RowParams::status.
+enum : int { STATUS_WAIT_TIMEOUT = 1 };
+
+}  // namespace gb300norm

@@ -1,0 +1,52 @@
+// launch.h -- internal interface between the C ABI (api.cu) and the
+// per-operation translation units that instantiate the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gb300norm.h"
+#include "common.cuh"
+
+namespace gb300norm {
+
+// Internal: "this kernel family cannot take the shape, try the next one".
+constexpr int NORM_ERR_UNSUPPORTED_INTERNAL = -1;
+
+// What the launchers need to know about the current device.
+struct DevInfo {
+  int dev = 0;
+  int sms = 0;               // streaming multiprocessors
+  int smem_optin = 0;        // max dynamic shared memory per CTA (opt-in)
+  int smem_per_sm = 0;       // shared memory per SM
+  int smem_reserved = 0;     // shared memory the system reserves per CTA
+  int64_t max_partial_rows = 0;  // dW/dB partial rows the workspace holds
+  int force_path = 0;        // 0 = automatic, 2 = always the loop kernels
+};
+
+// Partial rows of the dW / dB workspace for M rows on a device with `sms`
+// SMs: at most two row-kernel CTAs per SM write one each.
+inline int64_t partial_rows(int64_t M, int sms) {
+  const int64_t cap = 2 * (int64_t)sms;
+  return M < cap ? M : cap;
+}
+
+// Row kernels.  `aligned`: every streamed row (inputs and outputs) starts on
+// a 16-byte boundary.  *grid receives the number of CTAs launched (= the
+// number of partial rows written when dW / dB are computed).
+int launch_op_rms_fwd(const RowParams&, int dtype, int wdtype, const DevInfo&, bool aligned, cudaStream_t, int* grid);
+int launch_op_rms_bwd(const RowParams&, int dtype, int wdtype, bool dw, const DevInfo&, bool aligned, cudaStream_t,
+                      int* grid);
+int launch_op_ln_fwd(const RowParams&, int dtype, int wdtype, const DevInfo&, bool aligned, cudaStream_t, int* grid);
+int launch_op_ln_bwd(const RowParams&, int dtype, int wdtype, bool dw, bool db, const DevInfo&, bool aligned,
+                     cudaStream_t, int* grid);
+int launch_op_fadd_fwd(const RowParams&, int dtype, int wdtype, const DevInfo&, bool aligned, cudaStream_t, int* grid);
+int launch_op_fadd_bwd(const RowParams&, int dtype, int wdtype, bool dw, const DevInfo&, bool aligned, cudaStream_t,
+                       int* grid);
+
+// Stage 2 of the dW / dB reduction: out[j] = sum over g < G of ws[g*N + j],
+// in increasing g, converted once to out_dtype.  ws_db / db may be null.
+int launch_colreduce(const float* ws_dw, void* dw, const float* ws_db, void* db, int G, int N, int out_dtype,
+                     cudaStream_t st);
+
+}  // namespace gb300norm
