@@ -172,9 +172,13 @@ class ClockSampler:
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
+            self.err = open(self.path + ".err", "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=self.f, stderr=subprocess.DEVNULL)
+                                         stdout=self.f, stderr=self.err)
+            t0 = time.time()   # start timing only once the sampler is producing lines
+            while time.time() - t0 < 5 and os.path.getsize(self.path) == 0 and self.proc.poll() is None:
+                time.sleep(0.05)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -187,6 +191,7 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
             self.f.close()
+            self.err.close()
 
     def summary(self):
         if not self.proc:
@@ -235,16 +240,23 @@ def oracle_step(host, rows):
 
 
 def cpu_baseline(host, target_s=10.0):
+    """The oracle on `rows` rows of every operation, repeated until about
+    target_s seconds of CPU time have been spent."""
     import oracle
     oracle.build()
     M = host["rms"]["x"].shape[0]
     rows = min(M, 16)
     dt, _ = oracle_step(host, rows)
     rows = int(min(M, max(16, rows * target_s / max(dt, 1e-3))))
-    dt, nbytes = oracle_step(host, rows)
-    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{rows} rows of each of the 6 operations at N={host['rms']['x'].shape[1]} "
-                      f"(single-threaded FP64 C oracle, {dt:.1f} s)"}
+    total, nbytes, reps = 0.0, 0, 0
+    while total < target_s or reps == 0:
+        dt, b = oracle_step(host, rows)
+        total += dt
+        nbytes += b
+        reps += 1
+    return {"value": nbytes / total / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows} rows of each of the 6 operations at N={host['rms']['x'].shape[1]}, "
+                      f"{reps} repetition(s), {total:.1f} s (single-threaded FP64 C oracle)"}
 
 
 # ---------------------------------------------------------------------------
@@ -292,14 +304,18 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--M", type=int, default=8192)
     ap.add_argument("--N", type=int, default=8192)
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ops", default=",".join(OPS),
+                    help="comma-separated subset of the step's operations (profiling)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the frozen timings, the e2e run and the CPU baseline (profiling)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -312,17 +328,27 @@ def main():
     import row_normalization_rmsnorm_gb300 as g
 
     M, N = args.M, args.N
+    ops = [o for o in args.ops.split(",") if o]
+    assert all(o in OPS for o in ops), ops
     host = host_inputs(M, N, seed=rank)
     wl = Workload(g, host, M, N)
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
+    scrub = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device="cuda").fill_(1.0)
+
+    def flush_l2():
+        # write a buffer larger than L2, then read another one: no line of
+        # the step's tensors survives, and the dirty lines of the write are
+        # evicted before (not during) the timed step
+        flush.zero_()
+        scrub.sum()
 
     def step(events=None):
-        flush.zero_()
+        flush_l2()
         if events is not None:
             events[0].record(stream)
-        for i, op in enumerate(OPS):
+        for i, op in enumerate(ops):
             wl.run(op, True, stream)
             if events is not None:
                 events[i + 1].record(stream)
@@ -331,7 +357,7 @@ def main():
         step()
     torch.cuda.synchronize()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(OPS) + 1)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(args.steps)]
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -341,27 +367,27 @@ def main():
             step(evs[k])
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
-    op_ms = {op: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)] for i, op in enumerate(OPS)}
+    op_ms = {op: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)] for i, op in enumerate(ops)}
     step_ms = [evs[k][0].elapsed_time(evs[k][-1]) for k in range(args.steps)]
     ms_step = sum(step_ms) / len(step_ms)
     if ws > 1:
         t = torch.tensor([ms_step], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms_step = float(t.item())
-    step_bytes = sum(op_bytes(op, M, N) for op in OPS)
+    step_bytes = sum(op_bytes(op, M, N) for op in ops)
     value = step_bytes * ws / (ms_step * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
 
     # per-operation figures, trainable (inside the timed steps) and frozen
     per_op = {}
-    for op in OPS:
+    for op in ops:
         us = 1e3 * statistics.mean(op_ms[op])
         b = op_bytes(op, M, N)
         per_op[op] = {"us": us, "GBps": b / us / 1e3, "frac": b / us / 1e3 / peak, "bytes": b}
-    for op in ("rms_bwd", "ln_bwd", "fadd_bwd"):
+    for op in ([] if args.no_extras else [o for o in ("rms_bwd", "ln_bwd", "fadd_bwd") if o in ops]):
         ts = []
-        for _ in range(max(5, args.steps // 2)):
-            flush.zero_()
+        for _ in range(max(5, min(50, args.steps // 2))):
+            flush_l2()
             a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             wl.run(op, False, stream)
@@ -372,7 +398,7 @@ def main():
         b = op_bytes(op, M, N, trainable=False)
         per_op[op + "_frozen"] = {"us": us, "GBps": b / us / 1e3, "frac": b / us / 1e3 / peak, "bytes": b}
 
-    dom = max(OPS, key=lambda op: per_op[op]["us"])
+    dom = max(ops, key=lambda op: per_op[op]["us"])
     prof = load_profile_traffic(dom, M, N)
     roofline = {"bound": "hbm", "kernel": f"{dom} (row kernel"
                 + (" + dW/dB column reduce)" if dom.endswith("_bwd") else ")"),
@@ -381,10 +407,10 @@ def main():
                 "algorithmic_bytes_per_call": per_op[dom]["bytes"]}
 
     # end to end: host buffers, copies inside the timed region
-    e2e = run_e2e(wl, stream, args.e2e_steps, M, N)
+    e2e = None if args.no_extras else run_e2e(wl, stream, args.e2e_steps, M, N, ops)
 
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not (args.no_cpu_baseline or args.no_extras):
         cpu = cpu_baseline(host)
 
     if rank == 0:
@@ -393,15 +419,16 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": f"bf16 {M}x{N} RMSNorm+LayerNorm+FusedAddRMSNorm fwd+bwd (trainable)",
-                       "M": M, "N": N, "ops": OPS,
-                       "l2": "flushed before every step (zero-fill of 2x L2); every tensor > L2",
+                       "M": M, "N": N, "ops": ops,
+                       "l2": "flushed before every step (zero-fill of 2x L2, then a read of another 2x L2 "
+                             "so the flush's dirty lines are written back before timing); every tensor > L2",
                        "timing": "CUDA events on the launching stream; flush excluded",
                        "wall_s_timed_region": wall, "parallelism": f"replicas x{ws}"},
             "roofline": roofline,
             "per_op": per_op,
             "e2e": e2e,
             "cpu_baseline": cpu,
-            "gpu_launches": args.steps * sum(launches_per_op(op) for op in OPS),
+            "gpu_launches": args.steps * sum(launches_per_op(op) for op in ops),
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
@@ -423,19 +450,19 @@ def load_profile_traffic(op, M, N):
         return None
 
 
-def run_e2e(wl, stream, steps, M, N):
+def run_e2e(wl, stream, steps, M, N, ops):
     """Same metric through the same calls, from pinned host buffers."""
     host_in = {k: torch.empty_like(wl.t[k], device="cpu").pin_memory()
-               for op in OPS for k in Workload.IN[op]}
+               for op in ops for k in Workload.IN[op]}
     for k, v in host_in.items():
         v.copy_(wl.t[k])
     host_out = {k: torch.empty_like(wl.t[k], device="cpu").pin_memory()
-                for op in OPS for k in Workload.OUT[op]}
+                for op in ops for k in Workload.OUT[op]}
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
 
     def one():
-        for op in OPS:
+        for op in ops:
             for k in Workload.IN[op]:
                 wl.t[k].copy_(host_in[k], non_blocking=True)
             wl.run(op, True, stream)
@@ -451,7 +478,7 @@ def run_e2e(wl, stream, steps, M, N):
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
-    step_bytes = sum(op_bytes(op, M, N) for op in OPS)
+    step_bytes = sum(op_bytes(op, M, N) for op in ops)
     return {"value": step_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 

@@ -212,12 +212,29 @@ GB300NORM_API int norm_fused_add_rms_bwd(const void *dy, int64_t dy_stride,
 GB300NORM_API int norm_device_status(int reset, int *value);
 
 /*
+ * The CUDA runtime error code (a cudaError_t value) behind the most recent
+ * NORM_ERR_CUDA returned to the calling thread, 0 if there was none, and its
+ * text (static string, never NULL).
+ */
+GB300NORM_API int norm_last_cuda_error(void);
+GB300NORM_API const char *norm_cuda_error_string(int code);
+
+/*
  * Test hook: mode 0 (default) lets each call pick its kernel family from the
  * arguments; mode 2 makes every subsequent call in the process use the
  * general (any alignment) row kernels, so tests can compare both families
  * on the same inputs.  Returns NORM_OK or NORM_ERR_ARG.
  */
 GB300NORM_API int norm_debug_set_path(int mode);
+
+/*
+ * Test hook for launch-shape sweeps: key 1 = 16-byte chunks per thread of the
+ * aligned-row kernels (1, 2 or 4), key 2 = maximum CTAs per SM, key 3 =
+ * maximum pipeline stages; value 0 restores the automatic choice.  Affects
+ * speed only, never results of the same kernel family except through the
+ * reduction tree shape.  Returns NORM_OK or NORM_ERR_ARG.
+ */
+GB300NORM_API int norm_debug_tune(int key, int value);
 
 #ifdef __cplusplus
 }

@@ -54,11 +54,11 @@ def _load():
     I = ctypes.c_int64
     D = ctypes.c_double
     lib.oracle_rms_fwd.argtypes = [I, I, P, P, D, D, P, P]
-    lib.oracle_rms_bwd.argtypes = [I, I, P, P, P, D, D, P, P, P]
+    lib.oracle_rms_bwd.argtypes = [I, I, P, P, P, D, D, P, P, P, P]
     lib.oracle_ln_fwd.argtypes = [I, I, P, P, P, D, D, P, P, P, P]
-    lib.oracle_ln_bwd.argtypes = [I, I, P, P, P, D, D, P, P, P, P]
+    lib.oracle_ln_bwd.argtypes = [I, I, P, P, P, D, D, P, P, P, P, P, P]
     lib.oracle_fused_add_rms_fwd.argtypes = [I, I, P, P, P, D, D, P, P, P]
-    lib.oracle_fused_add_rms_bwd.argtypes = [I, I, P, P, P, P, D, D, P, P, P]
+    lib.oracle_fused_add_rms_bwd.argtypes = [I, I, P, P, P, P, D, D, P, P, P, P]
     lib.oracle_round_array.argtypes = [P, I, ctypes.c_int, P]
     lib.oracle_round_bf16.argtypes = [D]
     lib.oracle_round_bf16.restype = ctypes.c_uint16
@@ -99,18 +99,20 @@ def rms_fwd(x, w, offset=0.0, eps=1e-6):
     return y, rstd
 
 
-def rms_bwd(x, dy, w, offset=0.0, eps=1e-6, compute_dw=True, with_scale=False):
-    """RMSNorm backward. Returns (dx, dw or None, dx_scale or None)."""
+def rms_bwd(x, dy, w, offset=0.0, eps=1e-6, compute_dw=True, with_scale=False, rstd=None):
+    """RMSNorm backward. rstd: the forward's saved statistic (None = recompute).
+    Returns (dx, dw or None, dx_scale or None)."""
     lib = _load()
     x = _in(x)
     M, N = x.shape
     dy = _in(dy, (M, N))
     w = _in(w, (N,))
+    rs = None if rstd is None else _in(rstd, (M,))
     dx = np.empty((M, N))
     dw = _opt(compute_dw, N)
     sc = _opt(with_scale, (M, N))
     lib.oracle_rms_bwd(M, N, _ptr(x), _ptr(dy), _ptr(w), offset, eps,
-                       _ptr(dx), _ptr(dw), _ptr(sc))
+                       _ptr(dx), _ptr(dw), _ptr(sc), _ptr(rs))
     return dx, dw, sc
 
 
@@ -131,19 +133,25 @@ def ln_fwd(x, w, b=None, offset=0.0, eps=1e-6, with_scale=False):
 
 
 def ln_bwd(x, dy, w, offset=0.0, eps=1e-6, compute_dw=True, compute_db=True,
-           with_scale=False):
-    """LayerNorm backward. Returns (dx, dw or None, db or None, dx_scale or None)."""
+           with_scale=False, mean=None, rstd=None):
+    """LayerNorm backward. mean / rstd: the forward's saved statistics (both
+    or neither; None = recompute). Returns (dx, dw or None, db or None,
+    dx_scale or None)."""
     lib = _load()
     x = _in(x)
     M, N = x.shape
     dy = _in(dy, (M, N))
     w = _in(w, (N,))
+    if (mean is None) != (rstd is None):
+        raise ValueError("mean and rstd go together")
+    mu = None if mean is None else _in(mean, (M,))
+    rs = None if rstd is None else _in(rstd, (M,))
     dx = np.empty((M, N))
     dw = _opt(compute_dw, N)
     db = _opt(compute_db, N)
     sc = _opt(with_scale, (M, N))
     lib.oracle_ln_bwd(M, N, _ptr(x), _ptr(dy), _ptr(w), offset, eps, _ptr(dx),
-                      _ptr(dw), _ptr(db), _ptr(sc))
+                      _ptr(dw), _ptr(db), _ptr(sc), _ptr(mu), _ptr(rs))
     return dx, dw, db, sc
 
 
@@ -163,8 +171,9 @@ def fused_add_rms_fwd(x, residual, w, offset=0.0, eps=1e-6):
 
 
 def fused_add_rms_bwd(h, dy, w, dh_out=None, offset=0.0, eps=1e-6,
-                      compute_dw=True, with_scale=False):
-    """FusedAddRMSNorm backward at saved rows h.
+                      compute_dw=True, with_scale=False, rstd=None):
+    """FusedAddRMSNorm backward from the saved rows h (as stored by the
+    forward) and the forward's rstd (None = recompute from h).
 
     Returns (dx, dw or None, dx_scale or None); dx is also the residual
     gradient.
@@ -175,11 +184,12 @@ def fused_add_rms_bwd(h, dy, w, dh_out=None, offset=0.0, eps=1e-6,
     dy = _in(dy, (M, N))
     w = _in(w, (N,))
     dho = None if dh_out is None else _in(dh_out, (M, N))
+    rs = None if rstd is None else _in(rstd, (M,))
     dx = np.empty((M, N))
     dw = _opt(compute_dw, N)
     sc = _opt(with_scale, (M, N))
     lib.oracle_fused_add_rms_bwd(M, N, _ptr(h), _ptr(dy), _ptr(dho), _ptr(w),
-                                 offset, eps, _ptr(dx), _ptr(dw), _ptr(sc))
+                                 offset, eps, _ptr(dx), _ptr(dw), _ptr(sc), _ptr(rs))
     return dx, dw, sc
 
 

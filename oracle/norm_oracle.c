@@ -20,15 +20,18 @@
  *   - The normalisation constant is rstd = 1 / sqrt(mean + eps) with eps
  *     inside the square root (the pages print no formula; this is the
  *     standard reading).  LayerNorm uses the biased (1/N) variance.
- *   - The backward entry points recompute rstd (and the mean) from their
- *     input rows in FP64; they take no saved statistics.
+ *   - The backward entry points take the statistics the forward saved (rstd,
+ *     and the mean for LayerNorm) as optional inputs; given NULL they
+ *     recompute them from their input rows in FP64.
  *   - Rounding of an FP64 result to bf16 / fp16 / fp32 is done once, directly
  *     from FP64, round-to-nearest, ties-to-even (oracle_round_*).
  *
  * Optional outputs named *_scale hold, per element, the magnitude of the
- * terms whose sum forms that output (for example rstd*(|g_j| + |xhat_j*c|)
- * for an RMSNorm input gradient).  The tests use them to bound FP32
- * cancellation error; they play no part in the outputs themselves.
+ * terms whose sum forms that output, where a row constant that is itself a
+ * sum (c = mean of g*xhat) contributes the mean of its terms' magnitudes
+ * (for an RMSNorm input gradient: rstd*(|g_j| + |xhat_j| * mean|g xhat|)).
+ * The tests use them to bound FP32 cancellation error; they play no part in
+ * the outputs themselves.
  */
 #include <math.h>
 #include <stdint.h>
@@ -79,10 +82,14 @@ void oracle_rms_fwd(int64_t M, int64_t N, const double *x, const double *w,
  * is w or w + offset ("fix(cutedsl): ...", PyTorch accuracy comparison: dW is
  * unchanged).  A NULL dw is the frozen-weight case of
  * "perf(norm): skip dW/dB calculation when parameters are frozen", Motivation.
+ * rstd_in: the statistic saved by the forward (length M), or NULL to
+ * recompute it from x.  The formula is applied with whichever rstd is used.
+ * dx_scale_j = rstd*(|g_j| + |xhat_j| * (1/N) sum_k |g_k xhat_k|): the size of
+ * the terms dx_j is formed from, with c replaced by the size of its terms.
  */
 void oracle_rms_bwd(int64_t M, int64_t N, const double *x, const double *dy,
                     const double *w, double offset, double eps, double *dx,
-                    double *dw, double *dx_scale)
+                    double *dw, double *dx_scale, const double *rstd_in)
 {
     if (dw)
         for (int64_t j = 0; j < N; ++j)
@@ -90,17 +97,21 @@ void oracle_rms_bwd(int64_t M, int64_t N, const double *x, const double *dy,
     for (int64_t i = 0; i < M; ++i) {
         const double *xr = x + i * N;
         const double *dyr = dy + i * N;
-        double r = row_rstd_rms(xr, N, eps);
-        double sgx = 0.0;
-        for (int64_t j = 0; j < N; ++j)
-            sgx += dyr[j] * (w[j] + offset) * (xr[j] * r);
+        double r = rstd_in ? rstd_in[i] : row_rstd_rms(xr, N, eps);
+        double sgx = 0.0, sgx_abs = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            double gx = dyr[j] * (w[j] + offset) * (xr[j] * r);
+            sgx += gx;
+            sgx_abs += fabs(gx);
+        }
         double c = sgx / (double)N;
+        double c_abs = sgx_abs / (double)N;
         for (int64_t j = 0; j < N; ++j) {
             double xhat = xr[j] * r;
             double g = dyr[j] * (w[j] + offset);
             dx[i * N + j] = r * (g - xhat * c);
             if (dx_scale)
-                dx_scale[i * N + j] = r * (fabs(g) + fabs(xhat * c));
+                dx_scale[i * N + j] = r * (fabs(g) + fabs(xhat) * c_abs);
             if (dw)
                 dw[j] += dyr[j] * xhat;
         }
@@ -162,10 +173,13 @@ void oracle_ln_fwd(int64_t M, int64_t N, const double *x, const double *w,
  *   db_j   = sum over rows of dy_j            (if db != NULL).
  * dw and db are independent, as on "perf(norm): skip dW/dB calculation when
  * parameters are frozen", Key Changes (layer_norm).
+ * mean_in / rstd_in: the statistics saved by the forward, or both NULL to
+ * recompute them from x.
  */
 void oracle_ln_bwd(int64_t M, int64_t N, const double *x, const double *dy,
                    const double *w, double offset, double eps, double *dx,
-                   double *dw, double *db, double *dx_scale)
+                   double *dw, double *db, double *dx_scale,
+                   const double *mean_in, const double *rstd_in)
 {
     if (dw)
         for (int64_t j = 0; j < N; ++j)
@@ -177,12 +191,20 @@ void oracle_ln_bwd(int64_t M, int64_t N, const double *x, const double *dy,
         const double *xr = x + i * N;
         const double *dyr = dy + i * N;
         double mu, r;
-        row_stats_ln(xr, N, eps, &mu, &r);
-        double sg = 0.0, sgx = 0.0;
+        if (mean_in && rstd_in) {
+            mu = mean_in[i];
+            r = rstd_in[i];
+        } else {
+            row_stats_ln(xr, N, eps, &mu, &r);
+        }
+        double sg = 0.0, sgx = 0.0, sg_abs = 0.0, sgx_abs = 0.0;
         for (int64_t j = 0; j < N; ++j) {
             double g = dyr[j] * (w[j] + offset);
+            double gx = g * ((xr[j] - mu) * r);
             sg += g;
-            sgx += g * ((xr[j] - mu) * r);
+            sgx += gx;
+            sg_abs += fabs(g);
+            sgx_abs += fabs(gx);
         }
         double mg = sg / (double)N;
         double mgx = sgx / (double)N;
@@ -191,7 +213,8 @@ void oracle_ln_bwd(int64_t M, int64_t N, const double *x, const double *dy,
             double g = dyr[j] * (w[j] + offset);
             dx[i * N + j] = r * (g - mg - xhat * mgx);
             if (dx_scale)
-                dx_scale[i * N + j] = r * (fabs(g) + fabs(mg) + fabs(xhat * mgx));
+                dx_scale[i * N + j] = r * (fabs(g) + sg_abs / (double)N
+                                           + fabs(xhat) * sgx_abs / (double)N);
             if (dw)
                 dw[j] += dyr[j] * xhat;
             if (db)
@@ -222,18 +245,22 @@ void oracle_fused_add_rms_fwd(int64_t M, int64_t N, const double *x,
 }
 
 /*
- * FusedAddRMSNorm backward, evaluated at the saved residual-stream rows h
- * (the kernel saves h rounded to the activation type, "fix(cutedsl): ...",
- * PyTorch accuracy comparison): the RMSNorm input gradient at h plus the
- * gradient dh_out that arrives on the residual-stream output (NULL = zero).
- * The result is both dx and dresidual, since h = x + residual.
+ * FusedAddRMSNorm backward from the forward's saved tensors: the residual
+ * stream h as the kernel stores it (rounded to the activation type --
+ * "fix(cutedsl): ...", PyTorch accuracy comparison: the backward uses a
+ * rounded saved residual) and the forward's rstd of the unrounded sum
+ * (rstd_in; NULL recomputes it from h).  The RMSNorm input-gradient formula
+ * is applied to those saved values and the gradient dh_out arriving on the
+ * residual-stream output (NULL = zero) is added.  The result is both dx and
+ * dresidual, since h = x + residual.
  */
 void oracle_fused_add_rms_bwd(int64_t M, int64_t N, const double *h,
                               const double *dy, const double *dh_out,
                               const double *w, double offset, double eps,
-                              double *dx, double *dw, double *dx_scale)
+                              double *dx, double *dw, double *dx_scale,
+                              const double *rstd_in)
 {
-    oracle_rms_bwd(M, N, h, dy, w, offset, eps, dx, dw, dx_scale);
+    oracle_rms_bwd(M, N, h, dy, w, offset, eps, dx, dw, dx_scale, rstd_in);
     if (dh_out) {
         for (int64_t i = 0; i < M * N; ++i) {
             dx[i] = dx[i] + dh_out[i];

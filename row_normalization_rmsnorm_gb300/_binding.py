@@ -50,13 +50,20 @@ SIGNATURES = {
                                 _F, _I, _I, _P], _I),
     "norm_device_status": ([_I, ctypes.POINTER(_I)], _I),
     "norm_debug_set_path": ([_I], _I),
+    "norm_debug_tune": ([_I, _I], _I),
+    "norm_last_cuda_error": ([], _I),
+    "norm_cuda_error_string": ([_I], ctypes.c_char_p),
 }
 
 
 class NormError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
-        super().__init__(f"{fn}: status {status} ({status_str(status)})")
+        msg = f"{fn}: status {status} ({status_str(status)})"
+        if status == NORM_ERR_CUDA:
+            code = lib.norm_last_cuda_error()
+            msg += f"; CUDA error {code}: {lib.norm_cuda_error_string(code).decode()}"
+        super().__init__(msg)
 
 
 def _load():
@@ -132,6 +139,10 @@ def norm_device_status(reset: bool = False) -> int:
 
 def norm_debug_set_path(mode: int):
     _check("norm_debug_set_path", lib.norm_debug_set_path(int(mode)))
+
+
+def norm_debug_tune(key: int, value: int):
+    _check("norm_debug_tune", lib.norm_debug_tune(int(key), int(value)))
 
 
 def norm_rms_fwd(x, w, y, rstd=None, offset=0.0, eps=1e-6, stream=None):

@@ -13,9 +13,19 @@ using namespace gb300norm;
 // Device status word: bounded waits that ran out set bits here.
 __device__ int g_norm_status;
 
+thread_local int t_last_cuda_error = 0;
+
+namespace gb300norm {
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return NORM_ERR_CUDA;
+}
+}  // namespace gb300norm
+
 namespace {
 
 std::atomic<int> g_force_path{0};
+std::atomic<int> g_tune[4] = {{0}, {0}, {0}, {0}};
 
 int elem_size(int dt) {
   switch (dt) {
@@ -43,25 +53,30 @@ DevCache g_dev;
 
 int get_device(DevInfo* out, int** status) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return NORM_ERR_CUDA;
-  if (dev < 0 || dev >= 64) return NORM_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 64) return cuda_fail(cudaErrorInvalidDevice);
   std::lock_guard<std::mutex> g(g_dev.mu);
   if (!g_dev.ready[dev]) {
     DevInfo di;
     di.dev = dev;
-    if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&di.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
-      return NORM_ERR_CUDA;
+    if ((e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+            cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&di.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess)
+      return cuda_fail(e);
     void* st = nullptr;
-    if (cudaGetSymbolAddress(&st, g_norm_status) != cudaSuccess) return NORM_ERR_CUDA;
+    if ((e = cudaGetSymbolAddress(&st, g_norm_status)) != cudaSuccess) return cuda_fail(e);
     g_dev.info[dev] = di;
     g_dev.status[dev] = static_cast<int*>(st);
     g_dev.ready[dev] = true;
   }
   *out = g_dev.info[dev];
   out->force_path = g_force_path.load();
+  out->tune_npt = g_tune[1].load();
+  out->tune_max_ctas = g_tune[2].load();
+  out->tune_max_stages = g_tune[3].load();
   if (status) *status = g_dev.status[dev];
   return NORM_OK;
 }
@@ -218,9 +233,19 @@ const char* norm_status_str(int status) {
 
 int norm_version(void) { return 10000; }
 
+int norm_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char* norm_cuda_error_string(int code) { return cudaGetErrorString(static_cast<cudaError_t>(code)); }
+
 int norm_debug_set_path(int mode) {
   if (mode != 0 && mode != 2) return NORM_ERR_ARG;
   g_force_path.store(mode);
+  return NORM_OK;
+}
+
+int norm_debug_tune(int key, int value) {
+  if (key < 1 || key > 3 || value < 0 || value > 64) return NORM_ERR_ARG;
+  g_tune[key].store(value);
   return NORM_OK;
 }
 
@@ -240,10 +265,11 @@ int norm_device_status(int reset, int* value) {
   DevInfo di;
   int* st = nullptr;
   RETURN_IF(get_device(&di, &st));
-  if (cudaDeviceSynchronize() != cudaSuccess) return NORM_ERR_CUDA;
-  if (cudaMemcpy(value, st, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return NORM_ERR_CUDA;
-  if (reset && cudaMemset(st, 0, sizeof(int)) != cudaSuccess) return NORM_ERR_CUDA;
-  if (reset && cudaDeviceSynchronize() != cudaSuccess) return NORM_ERR_CUDA;
+  cudaError_t e;
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaMemcpy(value, st, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e);
+  if (reset && (e = cudaMemset(st, 0, sizeof(int))) != cudaSuccess) return cuda_fail(e);
+  if (reset && (e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e);
   return NORM_OK;
 }
 
@@ -367,6 +393,7 @@ int norm_rms_bwd(const void* dy, int64_t dy_stride, const void* x, int64_t x_str
                      vec_span(need ? workspace : nullptr, need, 1, true)};
   RETURN_IF(check_overlaps(sp, 7));
   if (!status) RETURN_IF(get_device(&di, &status));
+  di.max_partial_rows = partial_rows(M, di.sms);
   RowParams p = base_params(M, N, offset, eps, w, status);
   p.in0 = x; p.s_in0 = x_stride;
   p.in1 = dy; p.s_in1 = dy_stride;
@@ -413,6 +440,7 @@ int norm_ln_bwd(const void* dy, int64_t dy_stride, const void* x, int64_t x_stri
                      vec_span(need ? workspace : nullptr, need, 1, true)};
   RETURN_IF(check_overlaps(sp, 9));
   if (!status) RETURN_IF(get_device(&di, &status));
+  di.max_partial_rows = partial_rows(M, di.sms);
   RowParams p = base_params(M, N, offset, eps, w, status);
   p.in0 = x; p.s_in0 = x_stride;
   p.in1 = dy; p.s_in1 = dy_stride;
@@ -456,6 +484,7 @@ int norm_fused_add_rms_bwd(const void* dy, int64_t dy_stride, const void* dh_out
                      vec_span(dw, N, dws, true), vec_span(need ? workspace : nullptr, need, 1, true)};
   RETURN_IF(check_overlaps(sp, 8));
   if (!status) RETURN_IF(get_device(&di, &status));
+  di.max_partial_rows = partial_rows(M, di.sms);
   RowParams p = base_params(M, N, offset, eps, w, status);
   p.in0 = h; p.s_in0 = h_stride;
   p.in1 = dy; p.s_in1 = dy_stride;

@@ -2,8 +2,9 @@
 //
 // The row kernels leave one FP32 partial row per CTA ([G][N]).  Each CTA of
 // this kernel owns 32 adjacent columns: its 8 warps sum interleaved subsets of
-// the partial rows (warp k takes rows k, k+8, ...), coalesced 128-byte row
-// segments, and warp 0 adds the 8 subtotals in order.  The order of every
+// the partial rows (warp k takes rows k, k+8, ..., in four independent
+// chains), coalesced 128-byte row segments, and warp 0 adds the 8 subtotals
+// in order.  The order of every
 // addition is fixed by (G, N), so dW / dB are bit-identical from run to run.
 // With G = 0 (no rows) the outputs are set to zero.
 #include "launch.h"
@@ -19,10 +20,18 @@ __global__ void __launch_bounds__(256) colreduce_kernel(const float* __restrict_
   const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
   const int col = blockIdx.x * 32 + lane;
   __shared__ float part[8][33];
-  float acc = 0.f;
+  // four independent chains per thread (rows grp, grp+8, grp+16, grp+24 of
+  // each block of 32), joined in a fixed order
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
   if (col < N) {
-    for (int g = grp; g < G; g += 8) acc = fadd(acc, ws[(int64_t)g * N + col]);
+    int g = grp;
+    for (; g + 24 < G; g += 32) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) a[u] = fadd(a[u], ws[(int64_t)(g + 8 * u) * N + col]);
+    }
+    for (int u = 0; g < G; g += 8, ++u) a[u] = fadd(a[u], ws[(int64_t)g * N + col]);
   }
+  const float acc = fadd(fadd(a[0], a[1]), fadd(a[2], a[3]));
   part[grp][lane] = acc;
   __syncthreads();
   if (grp == 0 && col < N) {
@@ -37,7 +46,7 @@ template <class TO>
 static int launch_cr(const float* a, void* da, const float* b, void* db, int G, int N, cudaStream_t st) {
   dim3 grid((unsigned)((N + 31) / 32), db ? 2u : 1u);
   colreduce_kernel<TO><<<grid, 256, 0, st>>>(a, static_cast<TO*>(da), b, static_cast<TO*>(db), G, N);
-  return cudaGetLastError() == cudaSuccess ? NORM_OK : NORM_ERR_CUDA;
+  return launch_status();
 }
 
 int launch_colreduce(const float* ws_dw, void* dw, const float* ws_db, void* db, int G, int N, int out_dtype,

@@ -65,6 +65,53 @@ template <class T> struct Vec16 {
   union { uint4 u; T e[16 / sizeof(T)]; };
 };
 
+// Unpack 16 bytes of T into VEC floats (exact) and pack VEC floats back,
+// rounding each to nearest-even: two elements per instruction for the
+// 16-bit types.
+template <class T> struct Pack16;
+template <> struct Pack16<float> {
+  static __device__ __forceinline__ void unpack(const uint4& u, float (&f)[4]) {
+    f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+  }
+  static __device__ __forceinline__ uint4 pack(const float (&f)[4]) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+  }
+};
+template <> struct Pack16<__nv_bfloat16> {
+  static __device__ __forceinline__ void word(uint32_t w, float& lo, float& hi) {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xffff0000u);
+  }
+  static __device__ __forceinline__ void unpack(const uint4& u, float (&f)[8]) {
+    word(u.x, f[0], f[1]); word(u.y, f[2], f[3]); word(u.z, f[4], f[5]); word(u.w, f[6], f[7]);
+  }
+  static __device__ __forceinline__ uint32_t two(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  static __device__ __forceinline__ uint4 pack(const float (&f)[8]) {
+    return make_uint4(two(f[0], f[1]), two(f[2], f[3]), two(f[4], f[5]), two(f[6], f[7]));
+  }
+};
+template <> struct Pack16<__half> {
+  static __device__ __forceinline__ void word(uint32_t w, float& lo, float& hi) {
+    __half2 h = *reinterpret_cast<__half2*>(&w);
+    float2 f = __half22float2(h);
+    lo = f.x; hi = f.y;
+  }
+  static __device__ __forceinline__ void unpack(const uint4& u, float (&f)[8]) {
+    word(u.x, f[0], f[1]); word(u.y, f[2], f[3]); word(u.z, f[4], f[5]); word(u.w, f[6], f[7]);
+  }
+  static __device__ __forceinline__ uint32_t two(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  static __device__ __forceinline__ uint4 pack(const float (&f)[8]) {
+    return make_uint4(two(f[0], f[1]), two(f[2], f[3]), two(f[4], f[5]), two(f[6], f[7]));
+  }
+};
+
 // ---------------------------------------------------------------------------
 // FP32 arithmetic with explicit rounding.  Every value a kernel writes is
 // computed through these, so the compiler cannot contract or reorder them
@@ -101,13 +148,19 @@ __device__ __forceinline__ void block_sum(float (&v)[NV], float* red, int& bank)
     for (int i = 0; i < NV; ++i) r[warp * NV + i] = v[i];
   }
   __syncthreads();
+  // Every warp reduces the same warp partials with the same butterfly, so
+  // every thread of the CTA ends with the same bits.
 #pragma unroll
-  for (int i = 0; i < NV; ++i) v[i] = r[i];
-  for (int k = 1; k < nw; ++k) {
-#pragma unroll
-    for (int i = 0; i < NV; ++i) v[i] = fadd(v[i], r[k * NV + i]);
-  }
+  for (int i = 0; i < NV; ++i) v[i] = (lane < nw) ? r[lane * NV + i] : 0.f;
+  warp_sum<NV>(v);
   bank ^= 1;
+}
+
+// Sum of VEC per-lane accumulators in a fixed tree order.
+template <int VEC>
+__device__ __forceinline__ float tree_sum(const float (&a)[VEC]) {
+  if constexpr (VEC == 4) return fadd(fadd(a[0], a[1]), fadd(a[2], a[3]));
+  else return fadd(fadd(fadd(a[0], a[1]), fadd(a[2], a[3])), fadd(fadd(a[4], a[5]), fadd(a[6], a[7])));
 }
 
 // 1/sqrt(m + eps).
@@ -137,14 +190,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// try_wait suspends the calling thread until the phase completes or the
+// suspend-time hint (ns) passes, so a waiting warp does not spin on the
+// issue slots its neighbours need.
+constexpr uint32_t kSuspendHintNs = 1000000;   // 1 ms
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "n"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -171,6 +229,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
+
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t pol;

@@ -40,23 +40,42 @@ template <> struct OpInfo<LN_BWD>   { static constexpr int NIN = 2; static const
 template <> struct OpInfo<FADD_FWD> { static constexpr int NIN = 2; static constexpr bool BWD = false; };
 template <> struct OpInfo<FADD_BWD> { static constexpr int NIN = 3; static constexpr bool BWD = true; };
 
-__device__ __forceinline__ float div_n(float s, int N) { return __fdiv_rn(s, (float)N); }
+// Mean of a row sum: multiplied by the FP32 reciprocal of N formed once per
+// kernel (within 1.5 ulp of the quotient).
+__device__ __forceinline__ float div_n(float s, float inv_n) { return fmul(s, inv_n); }
 
 // ===========================================================================
 // Staged (TMA bulk copy) kernel
 // ===========================================================================
 constexpr int kStagedHeader = 1024;   // bytes: S mbarriers (<= 32) + reduction banks
 constexpr int kMaxStages = 16;
+// W' (and the bias) live in registers; the shared-memory layout keeps a
+// slot for them (size 0 here) so the column store can move there.
+constexpr bool kStagedWReg = true;
+
+// Shared memory for per-column values (W', and the LayerNorm bias) when they
+// are kept in shared memory rather than registers.
+template <int OP>
+__host__ __device__ constexpr size_t staged_col_bytes(int N, bool wreg) {
+  return wreg ? 0 : ((size_t)N * 4 * (OP == LN_FWD ? 2 : 1) + 127) / 128 * 128;
+}
 
 template <int OP, class T, class TW, int NPT, bool DW, bool DB>
 __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const int S) {
   constexpr int VEC = 16 / (int)sizeof(T);
   constexpr bool LN = (OP == LN_FWD || OP == LN_BWD);
   constexpr bool BWD = OpInfo<OP>::BWD;
-  constexpr int NB = (OP == LN_FWD) ? NPT : 1;   // bias registers
+  constexpr bool WREG = kStagedWReg;             // W' (and bias) in registers
+  // LayerNorm and FusedAdd forwards keep their FP32 row in registers between
+  // passes; RMSNorm re-reads it from the stage (fewer registers, more CTAs).
+  constexpr bool KEEP = !BWD && OP != RMS_FWD;
+  constexpr int NWR = WREG ? NPT : 1;
+  constexpr int NB = (OP == LN_FWD && WREG) ? NPT : 1;   // bias registers
   constexpr int NDW = DW ? NPT : 1;
   constexpr int NDB = DB ? NPT : 1;
+  constexpr int NX = KEEP ? NPT : 1;             // forward rows kept in registers
   constexpr int NR = (OP == LN_BWD) ? 2 : 1;     // values reduced per backward row
+  using P = Pack16<T>;
   const int N = p.N;
   const int nchunks = N / VEC;
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -67,7 +86,8 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   float* red = reinterpret_cast<float*>(smem + 256);
-  unsigned char* stages = smem + kStagedHeader;
+  float* wsm = reinterpret_cast<float*>(smem + kStagedHeader);   // W' [N] (+ bias [N]) when !WREG
+  unsigned char* stages = smem + kStagedHeader + staged_col_bytes<OP>(N, WREG);
   // abort_flag[k & 1] is raised while row k is awaited and read after row
   // k's barrier, so a thread already waiting for row k+1 cannot change what
   // the others read for row k.
@@ -75,7 +95,7 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
 
   // Per-thread constant columns: W' = float(w) + offset (and the LayerNorm
   // bias) in FP32, formed once per CTA.
-  float wv[NPT][VEC];
+  float wv[NWR][VEC];
   float bv[NB][VEC];
   const bool has_b = (OP == LN_FWD) && p.b != nullptr;
   const TW* wp = static_cast<const TW*>(p.w);
@@ -84,11 +104,31 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
     const int c = tid + j * nt;
 #pragma unroll
     for (int v = 0; v < VEC; ++v) {
-      wv[j][v] = (c < nchunks) ? fadd(to_f(wp[c * VEC + v]), p.offset) : 0.f;
-      if constexpr (OP == LN_FWD)
-        bv[j][v] = (has_b && c < nchunks) ? to_f(static_cast<const TW*>(p.b)[c * VEC + v]) : 0.f;
+      const float wj = (c < nchunks) ? fadd(to_f(wp[c * VEC + v]), p.offset) : 0.f;
+      const float bj = (has_b && c < nchunks) ? to_f(static_cast<const TW*>(p.b)[c * VEC + v]) : 0.f;
+      if constexpr (WREG) {
+        wv[j][v] = wj;
+        if constexpr (OP == LN_FWD) bv[j][v] = bj;
+      } else if (c < nchunks) {
+        wsm[c * VEC + v] = wj;
+        if constexpr (OP == LN_FWD) wsm[N + c * VEC + v] = bj;
+      }
     }
   }
+  // W' (or the bias) of chunk c, slot j, into w[VEC]
+  auto colv = [&](int j, int c, int which, float (&w)[VEC]) {
+    if constexpr (WREG) {
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) w[v] = which ? bv[NB > 1 ? j : 0][v] : wv[j][v];
+    } else {
+      const float4* q = reinterpret_cast<const float4*>(wsm + (which ? N : 0) + c * VEC);
+#pragma unroll
+      for (int v = 0; v < VEC; v += 4) {
+        const float4 t = q[v / 4];
+        w[v] = t.x; w[v + 1] = t.y; w[v + 2] = t.z; w[v + 3] = t.w;
+      }
+    }
+  };
   float dwa[NDW][VEC];
   float dba[NDB][VEC];
 #pragma unroll
@@ -115,36 +155,62 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
   const char* g0 = static_cast<const char*>(p.in0);
   const char* g1 = static_cast<const char*>(p.in1);
   const char* g2 = static_cast<const char*>(p.in2);
-  int64_t issued = 0;   // rows of this CTA whose copies have been issued (thread 0)
+  const float inv_n = 1.0f / (float)N;
+  // Producer state (thread 0): rows of this CTA whose copies have been
+  // issued, and the stage the next one goes to.  Stage and phase indices
+  // advance by counting, never by dividing the row index.
+  int64_t issued = 0;
+  int istage = 0;
 
-  auto issue = [&](int64_t k) {
-    const int s = (int)(k % S);
-    const int64_t row = row0 + k * G;
-    unsigned char* dst = stages + (size_t)s * stage_bytes;
+  auto issue_next = [&]() {
+    const int64_t row = row0 + issued * G;
+    unsigned char* dst = stages + (size_t)istage * stage_bytes;
+    uint64_t* bar = &bars[istage];
     fence_proxy_async_smem();
-    mbar_arrive_expect_tx(&bars[s], stage_bytes);
-    bulk_g2s(dst, g0 + row * p.s_in0 * (int64_t)sizeof(T), row_bytes, &bars[s], pol);
-    if (nin > 1) bulk_g2s(dst + row_bytes, g1 + row * p.s_in1 * (int64_t)sizeof(T), row_bytes, &bars[s], pol);
-    if (nin > 2) bulk_g2s(dst + 2 * row_bytes, g2 + row * p.s_in2 * (int64_t)sizeof(T), row_bytes, &bars[s], pol);
+    mbar_arrive_expect_tx(bar, stage_bytes);
+    bulk_g2s(dst, g0 + row * p.s_in0 * (int64_t)sizeof(T), row_bytes, bar, pol);
+    if (nin > 1) bulk_g2s(dst + row_bytes, g1 + row * p.s_in1 * (int64_t)sizeof(T), row_bytes, bar, pol);
+    if (nin > 2) bulk_g2s(dst + 2 * row_bytes, g2 + row * p.s_in2 * (int64_t)sizeof(T), row_bytes, bar, pol);
+    ++issued;
+    if (++istage == S) istage = 0;
   };
   if (tid == 0) {
-    for (; issued < nrows && issued < S - 1; ++issued) issue(issued);
+    while (issued < nrows && issued < S - 1) issue_next();
+  }
+
+  // Saved statistics of the backward are read one row ahead, off the
+  // critical path of the row being processed.
+  const bool have_stats = BWD && p.rstd_in != nullptr;
+  float rs_next = 0.f, mu_next = 0.f;
+  if (have_stats) {
+    rs_next = p.rstd_in[row0];
+    if constexpr (LN) mu_next = p.mean_in[row0];
   }
 
   int bank = 0;
   int64_t k = 0;
+  int s = 0;            // stage of row k
+  uint32_t phase = 0;   // parity of that stage's current use
   bool aborted = false;
-  for (; k < nrows; ++k) {
+  for (; k < nrows; ++k, (++s == S) ? (s = 0, phase ^= 1u) : 0) {
     const int64_t row = row0 + k * G;
-    const int s = (int)(k % S);
     const int fl = (int)(k & 1);
-    if (!mbar_wait_bounded(&bars[s], (uint32_t)((k / S) & 1))) {
+    float mean = 0.f, rstd = 0.f;
+    if (have_stats) {
+      rstd = rs_next;
+      mean = mu_next;
+      if (k + 1 < nrows) {
+        rs_next = p.rstd_in[row + G];
+        if constexpr (LN) mu_next = p.mean_in[row + G];
+      }
+    }
+    if (!mbar_wait_bounded(&bars[s], phase)) {
       atomicOr(p.status, STATUS_WAIT_TIMEOUT);
       abort_flag[fl] = 1;
     }
-    const T* r0 = reinterpret_cast<const T*>(stages + (size_t)s * stage_bytes);
-    const T* r1 = r0 + N;
-    const T* r2 = r1 + N;
+    const uint4* r0 = reinterpret_cast<const uint4*>(stages + (size_t)s * stage_bytes);
+    const uint4* r1 = r0 + nchunks;
+    const uint4* r2 = r1 + nchunks;
 
     // After the first barrier of row k every thread has finished row k-1, so
     // its stage can take the copy of row k+S-1.
@@ -152,77 +218,78 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
     auto after_first_barrier = [&]() {
       if (refilled) return;
       refilled = true;
-      if (tid == 0 && !abort_flag[fl] && issued < nrows) { issue(issued); ++issued; }
+      if (tid == 0 && !abort_flag[fl] && issued < nrows) issue_next();
     };
 
-    // ---- row statistics -------------------------------------------------
-    float mean = 0.f, rstd = 0.f;
-    const bool need_stats = !BWD || p.rstd_in == nullptr;
-    if (!need_stats) {
-      rstd = p.rstd_in[row];
-      if constexpr (LN) mean = p.mean_in[row];
-    } else if constexpr (LN) {
-      float a[1] = {0.f};
+    if constexpr (!BWD) {
+      // ---- forward: the row (x, or h = x + residual) in FP32 -------------
+      // row value of chunk c: x, or h = x + residual (FP32, exact for 16-bit
+      // inputs); kept in registers (xf) or re-read from the stage
+      auto rowv = [&](int c, float (&o)[VEC]) {
+        P::unpack(r0[c], o);
+        if constexpr (OP == FADD_FWD) {
+          float rf[VEC];
+          P::unpack(r1[c], rf);
 #pragma unroll
-      for (int j = 0; j < NPT; ++j) {
-        const int c = tid + j * nt;
-        if (c < nchunks) {
-          Vec16<T> xv; xv.u = reinterpret_cast<const uint4*>(r0)[c];
-#pragma unroll
-          for (int v = 0; v < VEC; ++v) a[0] = fadd(a[0], to_f(xv.e[v]));
+          for (int v = 0; v < VEC; ++v) o[v] = fadd(o[v], rf[v]);
         }
-      }
-      block_sum<1>(a, red, bank);
-      after_first_barrier();
-      mean = div_n(a[0], N);
-      float q[1] = {0.f};
+      };
+      float xf[NX][VEC];
+      float acc[VEC];
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
         const int c = tid + j * nt;
         if (c < nchunks) {
-          Vec16<T> xv; xv.u = reinterpret_cast<const uint4*>(r0)[c];
+          float t[VEC];
+          rowv(c, t);
+          if constexpr (OP == FADD_FWD) {
+            // the residual stream passed on: h rounded once to T
+            st_global_cs16(static_cast<T*>(p.out1) + row * p.s_out1 + (int64_t)c * VEC, P::pack(t));
+          }
 #pragma unroll
           for (int v = 0; v < VEC; ++v) {
-            const float d = fsub(to_f(xv.e[v]), mean);
-            q[0] = ffma(d, d, q[0]);
+            if constexpr (KEEP) xf[j][v] = t[v];
+            if constexpr (LN) acc[v] = fadd(acc[v], t[v]);
+            else              acc[v] = ffma(t[v], t[v], acc[v]);
           }
+        } else if constexpr (KEEP) {
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) xf[j][v] = 0.f;
         }
       }
-      block_sum<1>(q, red, bank);
-      rstd = inv_rms(div_n(q[0], N), p.eps);
-    } else {
-      float a[1] = {0.f};
-#pragma unroll
-      for (int j = 0; j < NPT; ++j) {
-        const int c = tid + j * nt;
-        if (c < nchunks) {
-          Vec16<T> xv; xv.u = reinterpret_cast<const uint4*>(r0)[c];
-          if constexpr (OP == FADD_FWD) {
-            Vec16<T> rv; rv.u = reinterpret_cast<const uint4*>(r1)[c];
-            Vec16<T> hv;
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) {
-              const float h = fadd(to_f(xv.e[v]), to_f(rv.e[v]));
-              a[0] = ffma(h, h, a[0]);
-              hv.e[v] = from_f<T>(h);      // the residual stream passed on, rounded once
-            }
-            st_global_cs16(static_cast<T*>(p.out1) + row * p.s_out1 + (int64_t)c * VEC, hv.u);
-          } else {
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) {
-              const float h = to_f(xv.e[v]);
-              a[0] = ffma(h, h, a[0]);
-            }
-          }
-        }
-      }
+      float a[1] = {tree_sum<VEC>(acc)};
       block_sum<1>(a, red, bank);
       after_first_barrier();
-      rstd = inv_rms(div_n(a[0], N), p.eps);
-    }
-
-    if constexpr (!BWD) {
-      // ---- forward outputs ----------------------------------------------
+      if constexpr (LN) {
+        mean = div_n(a[0], inv_n);
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+#pragma unroll
+        for (int j = 0; j < NPT; ++j) {
+          const int c = tid + j * nt;
+          if (c < nchunks) {
+            float t[VEC];
+            if constexpr (KEEP) {
+#pragma unroll
+              for (int v = 0; v < VEC; ++v) t[v] = xf[j][v];
+            } else {
+              rowv(c, t);
+            }
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+              const float d = fsub(t[v], mean);
+              acc[v] = ffma(d, d, acc[v]);
+            }
+          }
+        }
+        float q[1] = {tree_sum<VEC>(acc)};
+        block_sum<1>(q, red, bank);
+        rstd = inv_rms(div_n(q[0], inv_n), p.eps);
+      } else {
+        rstd = inv_rms(div_n(a[0], inv_n), p.eps);
+      }
       if (abort_flag[fl]) { aborted = true; break; }
       if (tid == 0) {
         if (p.rstd_out) p.rstd_out[row] = rstd;
@@ -233,83 +300,135 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
       for (int j = 0; j < NPT; ++j) {
         const int c = tid + j * nt;
         if (c < nchunks) {
-          Vec16<T> xv; xv.u = reinterpret_cast<const uint4*>(r0)[c];
-          Vec16<T> rv;
-          if constexpr (OP == FADD_FWD) rv.u = reinterpret_cast<const uint4*>(r1)[c];
-          Vec16<T> yv;
+          float t[VEC], w[VEC], yf[VEC];
+          if constexpr (KEEP) {
 #pragma unroll
-          for (int v = 0; v < VEC; ++v) {
-            float xf = to_f(xv.e[v]);
-            if constexpr (OP == FADD_FWD) xf = fadd(xf, to_f(rv.e[v]));
-            float yf;
-            if constexpr (OP == LN_FWD) yf = fadd(fmul(fmul(fsub(xf, mean), rstd), wv[j][v]), bv[j][v]);
-            else                        yf = fmul(fmul(xf, rstd), wv[j][v]);
-            yv.e[v] = from_f<T>(yf);
+            for (int v = 0; v < VEC; ++v) t[v] = xf[j][v];
+          } else {
+            rowv(c, t);
           }
-          st_global_cs16(yrow + (int64_t)c * VEC, yv.u);
+          colv(j, c, 0, w);
+          if constexpr (OP == LN_FWD) {
+            float bb[VEC];
+            colv(j, c, 1, bb);
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) yf[v] = ffma(fmul(fsub(t[v], mean), rstd), w[v], bb[v]);
+          } else {
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) yf[v] = fmul(fmul(t[v], rstd), w[v]);
+          }
+          st_global_cs16(yrow + (int64_t)c * VEC, P::pack(yf));
         }
       }
     } else {
-      // ---- backward: row sums of g (LayerNorm) and g*xhat -----------------
-      float a[NR];
+      // ---- backward -------------------------------------------------------
+      if (!have_stats) {
+        // statistics recomputed from the saved row (same arithmetic as the
+        // forward: two passes for LayerNorm)
+        float acc[VEC];
 #pragma unroll
-      for (int i = 0; i < NR; ++i) a[i] = 0.f;
+        for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+#pragma unroll
+        for (int j = 0; j < NPT; ++j) {
+          const int c = tid + j * nt;
+          if (c < nchunks) {
+            float xf[VEC];
+            P::unpack(r0[c], xf);
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+              if constexpr (LN) acc[v] = fadd(acc[v], xf[v]);
+              else              acc[v] = ffma(xf[v], xf[v], acc[v]);
+            }
+          }
+        }
+        float a[1] = {tree_sum<VEC>(acc)};
+        block_sum<1>(a, red, bank);
+        after_first_barrier();
+        if constexpr (LN) {
+          mean = div_n(a[0], inv_n);
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+#pragma unroll
+          for (int j = 0; j < NPT; ++j) {
+            const int c = tid + j * nt;
+            if (c < nchunks) {
+              float xf[VEC];
+              P::unpack(r0[c], xf);
+#pragma unroll
+              for (int v = 0; v < VEC; ++v) {
+                const float d = fsub(xf[v], mean);
+                acc[v] = ffma(d, d, acc[v]);
+              }
+            }
+          }
+          float q[1] = {tree_sum<VEC>(acc)};
+          block_sum<1>(q, red, bank);
+          rstd = inv_rms(div_n(q[0], inv_n), p.eps);
+        } else {
+          rstd = inv_rms(div_n(a[0], inv_n), p.eps);
+        }
+      }
+      // row sums of g (LayerNorm) and g * xhat
+      float acc0[VEC], acc1[VEC];
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) { acc0[v] = 0.f; acc1[v] = 0.f; }
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
         const int c = tid + j * nt;
         if (c < nchunks) {
-          Vec16<T> xv; xv.u = reinterpret_cast<const uint4*>(r0)[c];
-          Vec16<T> dv; dv.u = reinterpret_cast<const uint4*>(r1)[c];
+          float xf[VEC], df[VEC], w[VEC];
+          P::unpack(r0[c], xf);
+          P::unpack(r1[c], df);
+          colv(j, c, 0, w);
 #pragma unroll
           for (int v = 0; v < VEC; ++v) {
-            const float xf = to_f(xv.e[v]);
-            const float g = fmul(to_f(dv.e[v]), wv[j][v]);
+            const float g = fmul(df[v], w[v]);
             if constexpr (LN) {
-              const float xh = fmul(fsub(xf, mean), rstd);
-              a[0] = fadd(a[0], g);
-              a[NR - 1] = ffma(g, xh, a[NR - 1]);
+              const float xh = fmul(fsub(xf[v], mean), rstd);
+              acc0[v] = fadd(acc0[v], g);
+              acc1[v] = ffma(g, xh, acc1[v]);
             } else {
-              const float xh = fmul(xf, rstd);
-              a[0] = ffma(g, xh, a[0]);
+              acc1[v] = ffma(g, fmul(xf[v], rstd), acc1[v]);
             }
           }
         }
       }
+      float a[NR];
+      if constexpr (LN) { a[0] = tree_sum<VEC>(acc0); a[NR - 1] = tree_sum<VEC>(acc1); }
+      else              { a[0] = tree_sum<VEC>(acc1); }
       block_sum<NR>(a, red, bank);
       after_first_barrier();
       if (abort_flag[fl]) { aborted = true; break; }
-      const float mg = LN ? div_n(a[0], N) : 0.f;
-      const float mgx = div_n(a[NR - 1], N);
+      const float mg = LN ? div_n(a[0], inv_n) : 0.f;
+      const float mgx = div_n(a[NR - 1], inv_n);
+      const bool has_dh = (OP == FADD_BWD) && nin > 2;
       T* dxrow = static_cast<T*>(p.out0) + row * p.s_out0;
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
         const int c = tid + j * nt;
         if (c < nchunks) {
-          Vec16<T> xv; xv.u = reinterpret_cast<const uint4*>(r0)[c];
-          Vec16<T> dv; dv.u = reinterpret_cast<const uint4*>(r1)[c];
-          Vec16<T> hv;
-          const bool has_dh = (OP == FADD_BWD) && nin > 2;
-          if (has_dh) hv.u = reinterpret_cast<const uint4*>(r2)[c];
-          Vec16<T> ov;
+          float xf[VEC], df[VEC], hf[VEC], of[VEC], w[VEC];
+          P::unpack(r0[c], xf);
+          P::unpack(r1[c], df);
+          if (has_dh) P::unpack(r2[c], hf);
+          colv(j, c, 0, w);
 #pragma unroll
           for (int v = 0; v < VEC; ++v) {
-            const float xf = to_f(xv.e[v]);
-            const float dyf = to_f(dv.e[v]);
-            const float g = fmul(dyf, wv[j][v]);
+            const float g = fmul(df[v], w[v]);
             float xh, dx;
             if constexpr (LN) {
-              xh = fmul(fsub(xf, mean), rstd);
-              dx = fmul(rstd, fsub(fsub(g, mg), fmul(xh, mgx)));
+              xh = fmul(fsub(xf[v], mean), rstd);
+              dx = fmul(rstd, ffma(-xh, mgx, fsub(g, mg)));
             } else {
-              xh = fmul(xf, rstd);
-              dx = fmul(rstd, fsub(g, fmul(xh, mgx)));
+              xh = fmul(xf[v], rstd);
+              dx = fmul(rstd, ffma(-xh, mgx, g));
             }
-            if (has_dh) dx = fadd(dx, to_f(hv.e[v]));
-            ov.e[v] = from_f<T>(dx);
-            if constexpr (DW) dwa[j][v] = ffma(dyf, xh, dwa[j][v]);
-            if constexpr (DB) dba[j][v] = fadd(dba[j][v], dyf);
+            if (has_dh) dx = fadd(dx, hf[v]);
+            of[v] = dx;
+            if constexpr (DW) dwa[j][v] = ffma(df[v], xh, dwa[j][v]);
+            if constexpr (DB) dba[j][v] = fadd(dba[j][v], df[v]);
           }
-          st_global_cs16(dxrow + (int64_t)c * VEC, ov.u);
+          st_global_cs16(dxrow + (int64_t)c * VEC, P::pack(of));
         }
       }
     }
@@ -317,9 +436,12 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
 
   if (aborted) {
     // Bounded drain of the copies still in flight into this CTA's shared
-    // memory, then leave without writing partial sums.
+    // memory (rows k .. issued-1), then leave without writing partial sums.
     if (tid == 0) {
-      for (int64_t kk = k; kk < issued; ++kk) (void)mbar_wait_bounded(&bars[kk % S], (uint32_t)((kk / S) & 1));
+      for (int64_t kk = k; kk < issued; ++kk) {
+        (void)mbar_wait_bounded(&bars[s], phase);
+        if (++s == S) { s = 0; phase ^= 1u; }
+      }
     }
     return;
   }
@@ -356,6 +478,7 @@ __global__ void __launch_bounds__(512) loop_kernel(const RowParams p) {
   int bank = 0;
   const TW* wp = static_cast<const TW*>(p.w);
   const TW* bp = static_cast<const TW*>(p.b);
+  const float inv_n = 1.0f / (float)N;
   float* wsw = nullptr;
   float* wsb = nullptr;
   if constexpr (DW) wsw = p.ws_dw + (int64_t)blockIdx.x * N;
@@ -381,14 +504,14 @@ __global__ void __launch_bounds__(512) loop_kernel(const RowParams p) {
       float a[1] = {0.f};
       for (int j = tid; j < N; j += nt) a[0] = fadd(a[0], to_f(x[j]));
       block_sum<1>(a, red, bank);
-      mean = div_n(a[0], N);
+      mean = div_n(a[0], inv_n);
       float q[1] = {0.f};
       for (int j = tid; j < N; j += nt) {
         const float d = fsub(to_f(x[j]), mean);
         q[0] = ffma(d, d, q[0]);
       }
       block_sum<1>(q, red, bank);
-      rstd = inv_rms(div_n(q[0], N), p.eps);
+      rstd = inv_rms(div_n(q[0], inv_n), p.eps);
     } else {
       float a[1] = {0.f};
       for (int j = tid; j < N; j += nt) {
@@ -397,7 +520,7 @@ __global__ void __launch_bounds__(512) loop_kernel(const RowParams p) {
         a[0] = ffma(h, h, a[0]);
       }
       block_sum<1>(a, red, bank);
-      rstd = inv_rms(div_n(a[0], N), p.eps);
+      rstd = inv_rms(div_n(a[0], inv_n), p.eps);
     }
 
     if constexpr (!BWD) {
@@ -415,7 +538,7 @@ __global__ void __launch_bounds__(512) loop_kernel(const RowParams p) {
         }
         const float wj = fadd(to_f(wp[j]), p.offset);
         float yf;
-        if constexpr (OP == LN_FWD) yf = fadd(fmul(fmul(fsub(xf, mean), rstd), wj), bp ? to_f(bp[j]) : 0.f);
+        if constexpr (OP == LN_FWD) yf = ffma(fmul(fsub(xf, mean), rstd), wj, bp ? to_f(bp[j]) : 0.f);
         else                        yf = fmul(fmul(xf, rstd), wj);
         o0[j] = from_f<T>(yf);
       }
@@ -436,8 +559,8 @@ __global__ void __launch_bounds__(512) loop_kernel(const RowParams p) {
         }
       }
       block_sum<NR>(a, red, bank);
-      const float mg = LN ? div_n(a[0], N) : 0.f;
-      const float mgx = div_n(a[NR - 1], N);
+      const float mg = LN ? div_n(a[0], inv_n) : 0.f;
+      const float mgx = div_n(a[NR - 1], inv_n);
       for (int j = tid; j < N; j += nt) {
         const float xf = to_f(x[j]);
         const float dyf = to_f(i1[j]);
@@ -445,10 +568,10 @@ __global__ void __launch_bounds__(512) loop_kernel(const RowParams p) {
         float xh, dx;
         if constexpr (LN) {
           xh = fmul(fsub(xf, mean), rstd);
-          dx = fmul(rstd, fsub(fsub(g, mg), fmul(xh, mgx)));
+          dx = fmul(rstd, ffma(-xh, mgx, fsub(g, mg)));
         } else {
           xh = fmul(xf, rstd);
-          dx = fmul(rstd, fsub(g, fmul(xh, mgx)));
+          dx = fmul(rstd, ffma(-xh, mgx, g));
         }
         if constexpr (OP == FADD_BWD) {
           if (i2) dx = fadd(dx, to_f(i2[j]));
@@ -466,28 +589,45 @@ __global__ void __launch_bounds__(512) loop_kernel(const RowParams p) {
 // Launch logic
 // ===========================================================================
 
-// Chunks of 16 bytes each thread of the staged kernel owns (0 = too wide).
-inline int staged_npt(int nchunks) {
-  if (nchunks <= 256) return 1;
-  if (nchunks <= 512) return 2;
-  if (nchunks <= 2048) return 4;
-  return 0;
+// Threads of a staged CTA owning NPT 16-byte chunks each (0 = too many).
+inline int staged_threads(int nchunks, int npt) {
+  int t = (nchunks + npt - 1) / npt;
+  t = ((t + 31) / 32) * 32;
+  if (t < 64) t = 64;
+  return t <= 512 ? t : 0;
 }
 
-// Allow a kernel the device's full opt-in dynamic shared memory, once per
-// (kernel, device).  The attribute is an upper bound only; occupancy follows
-// the size actually launched.
-inline bool allow_max_smem(const void* fn, const DevInfo& di) {
+// Per-(kernel, device) facts, queried once: the kernel is allowed the
+// device's full opt-in shared memory (minus its own static shared memory) as
+// dynamic shared memory -- an upper bound only; occupancy follows the size
+// actually launched -- and its register-spill (local memory) size is kept
+// for the launch-shape choice.
+struct KernelInfo {
+  int max_dyn = -1;     // largest dynamic shared memory allowed, -1 = error
+  int local_bytes = 0;  // local memory per thread (register spills)
+};
+
+inline KernelInfo kernel_info(const void* fn, const DevInfo& di) {
   static std::mutex mu;
-  static std::map<std::pair<const void*, int>, bool> done;
+  static std::map<std::pair<const void*, int>, KernelInfo> done;
   std::lock_guard<std::mutex> g(mu);
   auto key = std::make_pair(fn, di.dev);
-  if (done.count(key)) return true;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin) != cudaSuccess)
-    return false;
-  done[key] = true;
-  return true;
+  auto it = done.find(key);
+  if (it != done.end()) return it->second;
+  KernelInfo ki;
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, fn);
+  if (e != cudaSuccess) { cuda_fail(e); return ki; }
+  const int max_dyn = di.smem_optin - (int)attr.sharedSizeBytes;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
+  if (e != cudaSuccess) { cuda_fail(e); return ki; }
+  ki.max_dyn = max_dyn;
+  ki.local_bytes = (int)attr.localSizeBytes;
+  done[key] = ki;
+  return ki;
 }
+
+inline int allow_max_smem(const void* fn, const DevInfo& di) { return kernel_info(fn, di).max_dyn; }
 
 // Cached occupancy query: resident CTAs per SM for (kernel, device, block, smem).
 inline int cached_occupancy(const void* fn, const DevInfo& di, int threads, size_t smem) {
@@ -499,9 +639,10 @@ inline int cached_occupancy(const void* fn, const DevInfo& di, int threads, size
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
   }
-  if (!allow_max_smem(fn, di)) return -1;
+  if (allow_max_smem(fn, di) < 0) return -1;
   int nb = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, threads, smem) != cudaSuccess) return -1;
+  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, threads, smem);
+  if (e != cudaSuccess) { cuda_fail(e); return -1; }
   std::lock_guard<std::mutex> g(mu);
   cache[key] = nb;
   return nb;
@@ -511,14 +652,16 @@ template <int OP, class T, class TW, int NPT, bool DW, bool DB>
 int launch_staged(const RowParams& p, const DevInfo& di, int nin, int max_ctas, cudaStream_t st, int* grid_out) {
   constexpr int VEC = 16 / (int)sizeof(T);
   const int nchunks = p.N / VEC;
-  int threads = (nchunks + NPT - 1) / NPT;
-  threads = ((threads + 31) / 32) * 32;
-  if (threads < 64) threads = 64;
+  const int threads = staged_threads(nchunks, NPT);
+  if (threads == 0) return NORM_ERR_UNSUPPORTED_INTERNAL;
   const size_t stage_bytes = (size_t)nin * p.N * sizeof(T);
   auto fn = staged_kernel<OP, T, TW, NPT, DW, DB>;
   const void* fp = reinterpret_cast<const void*>(fn);
-  const size_t min_smem = kStagedHeader + 2 * stage_bytes;
-  if (min_smem > (size_t)di.smem_optin) return NORM_ERR_UNSUPPORTED_INTERNAL;
+  const size_t fixed = kStagedHeader + staged_col_bytes<OP>(p.N, kStagedWReg);
+  const size_t min_smem = fixed + 2 * stage_bytes;
+  const int max_dyn = allow_max_smem(fp, di);
+  if (max_dyn < 0) return NORM_ERR_CUDA;
+  if (min_smem > (size_t)max_dyn) return NORM_ERR_UNSUPPORTED_INTERNAL;
   // Registers (and the 2-stage minimum) bound the CTAs per SM; shared memory
   // is then split evenly among them, as many stages as fit (<= kMaxStages).
   int nb = cached_occupancy(fp, di, threads, min_smem);
@@ -530,13 +673,14 @@ int launch_staged(const RowParams& p, const DevInfo& di, int nin, int max_ctas, 
   for (; ctas >= 1; --ctas) {
     size_t per_cta = (size_t)di.smem_per_sm / ctas;
     per_cta = per_cta > (size_t)di.smem_reserved + 64 ? per_cta - di.smem_reserved - 64 : 0;
-    if (per_cta > (size_t)di.smem_optin) per_cta = di.smem_optin;
+    if (per_cta > (size_t)max_dyn) per_cta = (size_t)max_dyn;
     if (per_cta < min_smem) continue;
-    S = (int)((per_cta - kStagedHeader) / stage_bytes);
+    S = (int)((per_cta - fixed) / stage_bytes);
     if (S > kMaxStages) S = kMaxStages;
+    if (di.tune_max_stages >= 2 && S > di.tune_max_stages) S = di.tune_max_stages;
     // confirm `ctas` CTAs of this size are resident together
     for (; S >= 2; --S) {
-      smem = kStagedHeader + (size_t)S * stage_bytes;
+      smem = fixed + (size_t)S * stage_bytes;
       const int fit = cached_occupancy(fp, di, threads, smem);
       if (fit < 0) return NORM_ERR_CUDA;
       if (fit >= ctas) break;
@@ -548,7 +692,7 @@ int launch_staged(const RowParams& p, const DevInfo& di, int nin, int max_ctas, 
   if (G > p.M) G = p.M;
   if ((DW || DB) && G > di.max_partial_rows) G = di.max_partial_rows;
   fn<<<(unsigned)G, threads, smem, st>>>(p, S);
-  if (cudaGetLastError() != cudaSuccess) return NORM_ERR_CUDA;
+  if (launch_status() != NORM_OK) return NORM_ERR_CUDA;
   *grid_out = (int)G;
   return NORM_OK;
 }
@@ -564,21 +708,70 @@ int launch_loop(const RowParams& p, const DevInfo& di, cudaStream_t st, int* gri
   if (G > p.M) G = p.M;
   if ((DW || DB) && G > di.max_partial_rows) G = di.max_partial_rows;
   fn<<<(unsigned)G, threads, 0, st>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return NORM_ERR_CUDA;
+  if (launch_status() != NORM_OK) return NORM_ERR_CUDA;
   *grid_out = (int)G;
   return NORM_OK;
 }
 
+// How well one staged instantiation suits a shape: fits at all, spills
+// registers, CTAs resident per SM (at the two-stage minimum), block size.
+struct StagedFit {
+  bool ok = false;
+  bool spills = false;
+  int ctas = 0;
+  int threads = 0;
+};
+
+template <int OP, class T, class TW, int NPT, bool DW, bool DB>
+StagedFit probe_staged(const RowParams& p, const DevInfo& di, int nin) {
+  constexpr int VEC = 16 / (int)sizeof(T);
+  StagedFit f;
+  f.threads = staged_threads(p.N / VEC, NPT);
+  if (f.threads == 0) return f;
+  const void* fp = reinterpret_cast<const void*>(staged_kernel<OP, T, TW, NPT, DW, DB>);
+  const KernelInfo ki = kernel_info(fp, di);
+  const size_t min_smem = kStagedHeader + staged_col_bytes<OP>(p.N, kStagedWReg) + 2 * (size_t)nin * p.N * sizeof(T);
+  if (ki.max_dyn < 0 || min_smem > (size_t)ki.max_dyn) return f;
+  const int nb = cached_occupancy(fp, di, f.threads, min_smem);
+  if (nb <= 0) return f;
+  f.ok = true;
+  f.spills = ki.local_bytes > 0;
+  f.ctas = nb;
+  return f;
+}
+
 // Row kernel for one (op, types, flags): the staged path when every streamed
-// row starts on a 16-byte boundary and fits, else the loop path.
+// row starts on a 16-byte boundary and fits, else the loop path.  Among the
+// staged shapes (1, 2 or 4 chunks per thread) the choice prefers, in order:
+// no register spills, at least two resident CTAs per SM (so one CTA's
+// barrier overlaps another's work), and blocks of about 256 threads.
 template <int OP, class T, class TW, bool DW, bool DB>
 int launch_rows(const RowParams& p, const DevInfo& di, bool rows_aligned, cudaStream_t st, int* grid_out) {
   constexpr int VEC = 16 / (int)sizeof(T);
   const int nin = (OP == FADD_BWD && p.in2 == nullptr) ? 2 : OpInfo<OP>::NIN;
-  const int max_ctas = (DW || DB) ? 2 : 4;
+  int max_ctas = (DW || DB) ? 2 : 4;
+  if (di.tune_max_ctas > 0) max_ctas = di.tune_max_ctas;
   if (rows_aligned && p.N % VEC == 0 && di.force_path != 2) {
+    // A backward picks its shape from the instantiation with every weight
+    // gradient on, whatever it computes itself: the block size fixes the
+    // reduction tree, so frozen and trainable calls give bit-identical dx.
+    constexpr bool PDW = OpInfo<OP>::BWD;
+    constexpr bool PDB = (OP == LN_BWD);
+    const StagedFit fits[3] = {probe_staged<OP, T, TW, 1, PDW, PDB>(p, di, nin),
+                               probe_staged<OP, T, TW, 2, PDW, PDB>(p, di, nin),
+                               probe_staged<OP, T, TW, 4, PDW, PDB>(p, di, nin)};
+    const int npts[3] = {1, 2, 4};
+    int best = -1;
+    long best_score = -1;
+    for (int i = 0; i < 3; ++i) {
+      if (!fits[i].ok) continue;
+      if (di.tune_npt && npts[i] != di.tune_npt) continue;
+      const int d = fits[i].threads > 256 ? fits[i].threads - 256 : 256 - fits[i].threads;
+      const long score = (fits[i].spills ? 0 : 1000000L) + (fits[i].ctas >= 2 ? 100000L : 0) + (1024 - d);
+      if (score > best_score) { best_score = score; best = i; }
+    }
     int rc = NORM_ERR_UNSUPPORTED_INTERNAL;
-    switch (staged_npt(p.N / VEC)) {
+    switch (best < 0 ? 0 : npts[best]) {
       case 1: rc = launch_staged<OP, T, TW, 1, DW, DB>(p, di, nin, max_ctas, st, grid_out); break;
       case 2: rc = launch_staged<OP, T, TW, 2, DW, DB>(p, di, nin, max_ctas, st, grid_out); break;
       case 4: rc = launch_staged<OP, T, TW, 4, DW, DB>(p, di, nin, max_ctas, st, grid_out); break;

@@ -13,6 +13,15 @@ namespace gb300norm {
 // Internal: "this kernel family cannot take the shape, try the next one".
 constexpr int NORM_ERR_UNSUPPORTED_INTERNAL = -1;
 
+// Remember `e` as this thread's last CUDA error; returns NORM_ERR_CUDA.
+int cuda_fail(cudaError_t e);
+
+// Launch status of the kernel just enqueued: NORM_OK or NORM_ERR_CUDA.
+inline int launch_status() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? NORM_OK : cuda_fail(e);
+}
+
 // What the launchers need to know about the current device.
 struct DevInfo {
   int dev = 0;
@@ -22,6 +31,10 @@ struct DevInfo {
   int smem_reserved = 0;     // shared memory the system reserves per CTA
   int64_t max_partial_rows = 0;  // dW/dB partial rows the workspace holds
   int force_path = 0;        // 0 = automatic, 2 = always the loop kernels
+  // test hooks (0 = automatic): staged chunks per thread, CTAs per SM, stages
+  int tune_npt = 0;
+  int tune_max_ctas = 0;
+  int tune_max_stages = 0;
 };
 
 // Partial rows of the dW / dB workspace for M rows on a device with `sms`

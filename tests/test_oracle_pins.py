@@ -221,6 +221,31 @@ def test_rms_matches_torch_float64(M, N, offset, eps):
     np.testing.assert_allclose(dw, gw.numpy(), rtol=1e-10, atol=1e-11)
     ms = (x * x).mean(axis=1)
     np.testing.assert_allclose(rstd, 1 / np.sqrt(ms + eps), rtol=1e-13)
+    # the saved-statistic path is the same computation
+    dxs, dws, _ = oracle.rms_bwd(x, dy, w, offset, eps, rstd=rstd)
+    np.testing.assert_array_equal(dxs, dx)
+    np.testing.assert_array_equal(dws, dw)
+
+
+def test_saved_statistics_enter_the_formula():
+    # a perturbed saved rstd moves dx as the formula says: with rstd' = s*rstd
+    # every term is rescaled, dx' = s*rstd*(g - s*xhat*s*c)
+    r = rng(77)
+    x, dy = r.standard_normal((3, 40)), r.standard_normal((3, 40))
+    w = 1 + 0.1 * r.standard_normal(40)
+    _, rstd = oracle.rms_fwd(x, w, 0.0, 1e-6)
+    s = 1.001
+    dx2, _, _ = oracle.rms_bwd(x, dy, w, 0.0, 1e-6, rstd=rstd * s)
+    rs = (rstd * s)[:, None]
+    xh = x * rs
+    g = dy * w
+    c = (g * xh).mean(axis=1, keepdims=True)
+    np.testing.assert_allclose(dx2, rs * (g - xh * c), rtol=1e-12, atol=1e-14)
+    _, mean, rstd_l, _ = oracle.ln_fwd(x, w, None, 0.0, 1e-6)
+    dxl, _, _, _ = oracle.ln_bwd(x, dy, w, 0.0, 1e-6, mean=mean + 0.01, rstd=rstd_l)
+    xh = (x - (mean + 0.01)[:, None]) * rstd_l[:, None]
+    expect = rstd_l[:, None] * (g - g.mean(1, keepdims=True) - xh * (g * xh).mean(1, keepdims=True))
+    np.testing.assert_allclose(dxl, expect, rtol=1e-11, atol=1e-13)
 
 
 @pytest.mark.parametrize("M,N", SHAPES[1:])
@@ -244,6 +269,10 @@ def test_ln_matches_torch_float64(M, N, with_bias, offset, eps):
     np.testing.assert_allclose(db, gb.numpy(), rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(mean, x.mean(axis=1), rtol=1e-13, atol=1e-14)
     np.testing.assert_allclose(rstd, 1 / np.sqrt(x.var(axis=1) + eps), rtol=1e-12)
+    dxs, dws, dbs, _ = oracle.ln_bwd(x, dy, w, offset, eps, mean=mean, rstd=rstd)
+    np.testing.assert_array_equal(dxs, dx)
+    np.testing.assert_array_equal(dws, dw)
+    np.testing.assert_array_equal(dbs, db)
 
 
 @pytest.mark.parametrize("M,N", SHAPES)
@@ -268,6 +297,10 @@ def test_fused_add_matches_torch_float64(M, N, offset):
     np.testing.assert_allclose(dx, gx.numpy(), rtol=1e-10, atol=1e-11)
     np.testing.assert_allclose(dx, gr.numpy(), rtol=1e-10, atol=1e-11)
     np.testing.assert_allclose(dw, gw.numpy(), rtol=1e-10, atol=1e-11)
+    # the forward's saved rstd gives the same result at the unrounded h
+    dxs, dws, _ = oracle.fused_add_rms_bwd(h, dy, w, dho, offset, eps, rstd=rstd)
+    np.testing.assert_array_equal(dxs, dx)
+    np.testing.assert_array_equal(dws, dw)
     # without a residual-output gradient it reduces to the RMSNorm backward
     dx0, dw0, _ = oracle.fused_add_rms_bwd(h, dy, w, None, offset, eps)
     dxr, dwr, _ = oracle.rms_bwd(h, dy, w, offset, eps)

@@ -72,7 +72,8 @@ def check_rms(out, case, label, offset=0.0, eps=EPS):
     for r0, r1 in blocks(M):
         x, dy = f64(case["x"][r0:r1]), f64(case["dy"][r0:r1])
         y, rstd = oracle.rms_fwd(x, w, offset, eps)
-        dx, dwb, sc = oracle.rms_bwd(x, dy, w, offset, eps, with_scale=True)
+        # the backward consumes the statistics its forward saved, as on the GPU
+        dx, dwb, sc = oracle.rms_bwd(x, dy, w, offset, eps, with_scale=True, rstd=rstd)
         tag = f"{label} rows {r0}:{r1}"
         check(out["y"].view[r0:r1], y, tn, label=f"{tag} y")
         check(out["rstd"][r0:r1], rstd, "float32", label=f"{tag} rstd")
@@ -112,7 +113,7 @@ def check_ln(out, case, label, offset=0.0, eps=EPS, bias=True):
     for r0, r1 in blocks(M):
         x, dy = f64(case["x"][r0:r1]), f64(case["dy"][r0:r1])
         y, mean, rstd, ysc = oracle.ln_fwd(x, w, b, offset, eps, with_scale=True)
-        dx, dwb, dbb, sc = oracle.ln_bwd(x, dy, w, offset, eps, with_scale=True)
+        dx, dwb, dbb, sc = oracle.ln_bwd(x, dy, w, offset, eps, with_scale=True, mean=mean, rstd=rstd)
         tag = f"{label} rows {r0}:{r1}"
         check(out["y"].view[r0:r1], y, tn, scale=ysc, label=f"{tag} y")
         check(out["mean"][r0:r1], mean, "float32", scale=16 * np.abs(x).mean(axis=1), label=f"{tag} mean")
@@ -148,8 +149,9 @@ def run_fadd(g, case, stride=None, offset=0.0, eps=EPS, dw_dtype=None, with_dh=T
 
 
 def check_fadd(out, case, label, offset=0.0, eps=EPS, with_dh=True):
-    """The backward is checked at the saved h as the oracle itself rounds it
-    (the forward stores h rounded to the activation type)."""
+    """The backward is checked from the forward's saved tensors as the
+    oracle itself forms them: h rounded to the activation type and the rstd
+    of the unrounded sum."""
     tn = dtype_name(out["y"].dtype)
     M, N = case["x"].shape
     w = f64(case["w"])
@@ -159,7 +161,7 @@ def check_fadd(out, case, label, offset=0.0, eps=EPS, with_dh=True):
         dh = f64(case["dh_out"][r0:r1]) if with_dh else None
         y, h, rstd = oracle.fused_add_rms_fwd(x, r, w, offset, eps)
         h_saved = rounded(h, tn)
-        dx, dwb, sc = oracle.fused_add_rms_bwd(h_saved, dy, w, dh, offset, eps, with_scale=True)
+        dx, dwb, sc = oracle.fused_add_rms_bwd(h_saved, dy, w, dh, offset, eps, with_scale=True, rstd=rstd)
         tag = f"{label} rows {r0}:{r1}"
         check(out["y"].view[r0:r1], y, tn, label=f"{tag} y")
         check(out["h"].view[r0:r1], h, tn, label=f"{tag} h_out")
