@@ -80,7 +80,8 @@ enum {
     NORM_ERR_VALUE = 7,     /* eps < 0, or eps / offset not finite              */
     NORM_ERR_ALIAS = 8,     /* an output overlaps an input in a way not allowed */
     NORM_ERR_CUDA = 9,      /* CUDA runtime error while querying or launching   */
-    NORM_ERR_ARG = 10       /* inconsistent optional arguments (see each call)  */
+    NORM_ERR_ARG = 10,      /* inconsistent optional arguments (see each call)  */
+    NORM_ERR_TOO_LARGE = 11 /* problem exceeds the library's fixed scratch      */
 };
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -200,6 +201,35 @@ GB300NORM_API int norm_fused_add_rms_bwd(const void *dy, int64_t dy_stride,
                            void *workspace, size_t workspace_bytes,
                            int64_t M, int64_t N, float offset, float eps,
                            int dtype, int w_dtype, gb300norm_stream_t stream);
+
+/*
+ * norm_rms_bwd_noalloc -- the RMSNorm backward of norm_rms_bwd for callers
+ * that cannot allocate device memory (no cudaMalloc where they run: inside an
+ * allocator-free runtime, a plugin whose host owns all device memory, or
+ * code that must not touch the allocator while a stream is being captured).
+ * The pages have no counterpart to this entry point.
+ *
+ * Same arguments, meaning and results as norm_rms_bwd, without workspace:
+ * the dW partial sums go to a fixed scratch array compiled into the library
+ * (norm_noalloc_scratch_bytes() bytes, 16 MiB), which every GPU that loads
+ * the library holds until the process exits.  A trainable call (dw != NULL)
+ * whose partial sums would not fit -- norm_bwd_workspace_bytes(M, N, 1, 0)
+ * larger than the scratch -- returns NORM_ERR_TOO_LARGE before anything is
+ * enqueued.  The first call on each device looks up the scratch's device
+ * address (with that device current) and caches it; make that first call
+ * before capturing a stream.  All calls on a device share the scratch, so
+ * calls whose kernels may overlap on the GPU (unordered streams) race and
+ * give wrong dW; order them on one stream or with events.  Nothing in the
+ * scratch has to be cleared: each call writes every value it reads.
+ */
+GB300NORM_API size_t norm_noalloc_scratch_bytes(void);
+GB300NORM_API int norm_rms_bwd_noalloc(const void *dy, int64_t dy_stride,
+                                       const void *x, int64_t x_stride,
+                                       const void *w, const float *rstd,
+                                       void *dx, int64_t dx_stride,
+                                       void *dw, int dw_dtype,
+                                       int64_t M, int64_t N, float offset, float eps,
+                                       int dtype, int w_dtype, gb300norm_stream_t stream);
 
 /*
  * Device-side status word shared by all kernels of this library on the

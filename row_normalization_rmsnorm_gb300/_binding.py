@@ -32,6 +32,7 @@ NORM_ERR_VALUE = 7
 NORM_ERR_ALIAS = 8
 NORM_ERR_CUDA = 9
 NORM_ERR_ARG = 10
+NORM_ERR_TOO_LARGE = 11
 
 # Every entry point the header declares, with its ctypes signature.
 _P, _I64, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -52,6 +53,8 @@ SIGNATURES = {
     "norm_debug_set_path": ([_I], _I),
     "norm_debug_tune": ([_I, _I], _I),
     "norm_last_cuda_error": ([], _I),
+    "norm_noalloc_scratch_bytes": ([], _SZ),
+    "norm_rms_bwd_noalloc": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _I, _I64, _I64, _F, _F, _I, _I, _P], _I),
     "norm_cuda_error_string": ([_I], ctypes.c_char_p),
 }
 
@@ -164,6 +167,17 @@ def norm_rms_bwd(dy, x, w, rstd, dx, dw=None, workspace=None, offset=0.0, eps=1e
                           _dev(workspace, "workspace"), ws_bytes, M, N, float(offset), float(eps),
                           DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream))
     _check("norm_rms_bwd", rc)
+
+
+def norm_rms_bwd_noalloc(dy, x, w, rstd, dx, dw=None, offset=0.0, eps=1e-6, stream=None):
+    """norm_rms_bwd without a workspace: the dW partial sums use the
+    library's fixed scratch (for callers that cannot allocate)."""
+    M, N = x.shape
+    rc = lib.norm_rms_bwd_noalloc(_dev(dy, "dy", 2), _rs(dy), _dev(x, "x", 2), _rs(x), _dev(w, "w", 1),
+                                  _dev(rstd, "rstd", 1), _dev(dx, "dx", 2), _rs(dx), _dev(dw, "dw", 1),
+                                  DTYPE_CODE[dw.dtype] if dw is not None else NORM_F32, M, N, float(offset),
+                                  float(eps), DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream))
+    _check("norm_rms_bwd_noalloc", rc)
 
 
 def norm_ln_fwd(x, w, b, y, mean=None, rstd=None, offset=0.0, eps=1e-6, stream=None):

@@ -227,6 +227,7 @@ const char* norm_status_str(int status) {
     case NORM_ERR_ALIAS: return "an output overlaps another argument in a way that is not allowed";
     case NORM_ERR_CUDA: return "CUDA runtime error while querying the device or launching";
     case NORM_ERR_ARG: return "inconsistent optional arguments";
+    case NORM_ERR_TOO_LARGE: return "problem too large for the library's fixed scratch (no-allocation entry point)";
     default: return "unknown status";
   }
 }

@@ -49,7 +49,7 @@ def test_binding_covers_exactly_the_header(g):
 
 
 def test_status_strings_and_version(g):
-    for code in range(0, 11):
+    for code in range(0, 12):
         s = g.status_str(code)
         assert s and s != "unknown status"
     assert g.status_str(99) == "unknown status"
