@@ -320,12 +320,13 @@ def main():
     if args.impl == "reference":
         return run_reference(args)
 
-    ws, rank, local = dist_env()
+    import row_normalization_rmsnorm_gb300 as g
+    from row_normalization_rmsnorm_gb300 import dist as gdist
+    ws, rank, local = gdist.rank_env()
     torch.cuda.set_device(local)
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    import row_normalization_rmsnorm_gb300 as g
 
     M, N = args.M, args.N
     ops = [o for o in args.ops.split(",") if o]
@@ -370,10 +371,7 @@ def main():
     op_ms = {op: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)] for i, op in enumerate(ops)}
     step_ms = [evs[k][0].elapsed_time(evs[k][-1]) for k in range(args.steps)]
     ms_step = sum(step_ms) / len(step_ms)
-    if ws > 1:
-        t = torch.tensor([ms_step], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = gdist.max_over_ranks(ms_step, device="cuda")
     step_bytes = sum(op_bytes(op, M, N) for op in ops)
     value = step_bytes * ws / (ms_step * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
