@@ -314,6 +314,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ops", default=",".join(OPS),
                     help="comma-separated subset of the step's operations (profiling)")
+    ap.add_argument("--no-shapes", action="store_true", help="skip the per-shape table")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the frozen timings, the e2e run and the CPU baseline (profiling)")
     args = ap.parse_args()
@@ -410,6 +411,7 @@ def main():
     cpu = None
     if rank == 0 and ws == 1 and not (args.no_cpu_baseline or args.no_extras):
         cpu = cpu_baseline(host)
+    shapes = None if (args.no_extras or args.no_shapes) else shape_table(g, flush_l2)
 
     if rank == 0:
         line = {
@@ -424,6 +426,7 @@ def main():
                        "wall_s_timed_region": wall, "parallelism": f"replicas x{ws}"},
             "roofline": roofline,
             "per_op": per_op,
+            "shapes": shapes,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gpu_launches": args.steps * sum(launches_per_op(op) for op in ops),
@@ -434,6 +437,85 @@ def main():
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
     return 0
+
+
+# Shapes the pages report on ("perf(norm): ...", Benchmark Results: the
+# frozen-parameter backward grid; "fix(cutedsl): ...", Benchmark results:
+# Gemma RMSNorm and FusedAddRMSNorm), timed one call at a time with a clean
+# L2, as context for the pages' numbers (other GPUs).
+GRID_SHAPES = [(2048, 4096), (4096, 4096), (4096, 8192), (8192, 4096), (8192, 8192)]
+GEMMA_SHAPES = [(1, 4096), (128, 4096), (2048, 4096), (8192, 4096), (128, 8192), (2048, 8192), (128, 18432)]
+FADD_SHAPES = [(128, 4096), (2048, 4096), (2048, 8192)]
+
+
+def shape_table(g, flush_l2, reps=40):
+    stream = torch.cuda.current_stream()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(0)
+
+    def timed(fn):
+        fn()
+        ts = []
+        for _ in range(reps):
+            flush_l2()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        # mean, not median: the event clock ticks in ~2 us steps here
+        return round(statistics.mean(ts), 2)
+
+    def tensors(M, N):
+        r = lambda: torch.randn(M, N, device="cuda", generator=gen).to(torch.bfloat16)  # noqa: E731
+        t = {"x": r(), "dy": r(), "res": r(), "dh": r(), "y": torch.empty(M, N, dtype=torch.bfloat16, device="cuda"),
+             "dx": torch.empty(M, N, dtype=torch.bfloat16, device="cuda"),
+             "h": torch.empty(M, N, dtype=torch.bfloat16, device="cuda"),
+             "w": (1 + 0.1 * torch.randn(N, device="cuda", generator=gen)).to(torch.bfloat16),
+             "b": (0.1 * torch.randn(N, device="cuda", generator=gen)).to(torch.bfloat16),
+             "rstd": torch.empty(M, device="cuda"), "mean": torch.empty(M, device="cuda"),
+             "dw": torch.empty(N, dtype=torch.bfloat16, device="cuda"),
+             "db": torch.empty(N, dtype=torch.bfloat16, device="cuda")}
+        t["ws"] = torch.empty(max(16, g.norm_bwd_workspace_bytes(M, N, True, True)), dtype=torch.uint8,
+                              device="cuda")
+        return t
+
+    rows = []
+    for M, N in GRID_SHAPES:
+        t = tensors(M, N)
+        for op in ("rms", "ln"):
+            if op == "rms":
+                fwd = lambda: g.norm_rms_fwd(t["x"], t["w"], t["y"], t["rstd"])  # noqa: E731
+                bwd = lambda tr: g.norm_rms_bwd(t["dy"], t["x"], t["w"], t["rstd"], t["dx"],  # noqa: E731
+                                                t["dw"] if tr else None, t["ws"] if tr else None)
+            else:
+                fwd = lambda: g.norm_ln_fwd(t["x"], t["w"], t["b"], t["y"], t["mean"], t["rstd"])  # noqa: E731
+                bwd = lambda tr: g.norm_ln_bwd(t["dy"], t["x"], t["w"], t["mean"], t["rstd"], t["dx"],  # noqa: E731
+                                               t["dw"] if tr else None, t["db"] if tr else None,
+                                               t["ws"] if tr else None)
+            fwd()
+            r = {"op": op, "M": M, "N": N, "fwd_us": timed(fwd), "bwd_us": timed(lambda: bwd(True)),
+                 "bwd_frozen_us": timed(lambda: bwd(False))}
+            r["bwd_frozen_GBps"] = round(op_bytes(op + "_bwd", M, N, trainable=False) / r["bwd_frozen_us"] / 1e3)
+            rows.append(r)
+        del t
+    for M, N in GEMMA_SHAPES:
+        t = tensors(M, N)
+        t["w"] = (0.01 * torch.randn(N, device="cuda", generator=gen)).to(torch.bfloat16)
+        fwd = lambda: g.norm_rms_fwd(t["x"], t["w"], t["y"], t["rstd"], 1.0)  # noqa: E731
+        both = lambda: (fwd(), g.norm_rms_bwd(t["dy"], t["x"], t["w"], t["rstd"], t["dx"], t["dw"],  # noqa: E731
+                                              t["ws"], 1.0))
+        rows.append({"op": "gemma_rms", "M": M, "N": N, "fwd_us": timed(fwd), "fwd_bwd_us": timed(both)})
+        del t
+    for M, N in FADD_SHAPES:
+        t = tensors(M, N)
+        fwd = lambda: g.norm_fused_add_rms_fwd(t["x"], t["res"], t["w"], t["y"], t["h"], t["rstd"], 1.0)  # noqa
+        both = lambda: (fwd(), g.norm_fused_add_rms_bwd(t["dy"], t["dh"], t["h"], t["w"], t["rstd"],  # noqa: E731
+                                                        t["dx"], t["dw"], t["ws"], 1.0))
+        rows.append({"op": "fadd_rms", "M": M, "N": N, "fwd_us": timed(fwd), "fwd_bwd_us": timed(both)})
+        del t
+    return rows
 
 
 def load_profile_traffic(op, M, N):

@@ -126,8 +126,8 @@ __device__ __forceinline__ float ffma(float a, float b, float c) { return __fmaf
 // ---------------------------------------------------------------------------
 // Reductions.  Butterfly shuffles give every lane the same sum (each step adds
 // the same two operands on both partners); warps are combined in a fixed
-// order.  `red` holds two banks of [32 warps][NV] floats used alternately so
-// that consecutive reductions need only one barrier each.
+// order.  `red` holds two banks of [32 warps][kMaxReduceValues] floats used
+// alternately so that consecutive reductions need only one barrier each.
 // ---------------------------------------------------------------------------
 template <int NV>
 __device__ __forceinline__ void warp_sum(float (&v)[NV]) {
@@ -137,12 +137,17 @@ __device__ __forceinline__ void warp_sum(float (&v)[NV]) {
     for (int i = 0; i < NV; ++i) v[i] = fadd(v[i], __shfl_xor_sync(0xffffffffu, v[i], o));
 }
 
+// Values one block_sum call may reduce; each bank has room for that many per
+// warp, whatever a given call uses, so consecutive calls never share slots.
+constexpr int kMaxReduceValues = 2;
+
 template <int NV>
 __device__ __forceinline__ void block_sum(float (&v)[NV], float* red, int& bank) {
+  static_assert(NV <= kMaxReduceValues, "bank size");
   warp_sum<NV>(v);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
-  float* r = red + bank * 32 * NV;
+  float* r = red + bank * 32 * kMaxReduceValues;
   if (lane == 0) {
 #pragma unroll
     for (int i = 0; i < NV; ++i) r[warp * NV + i] = v[i];

@@ -49,9 +49,9 @@ __device__ __forceinline__ float div_n(float s, float inv_n) { return fmul(s, in
 // ===========================================================================
 constexpr int kStagedHeader = 1024;   // bytes: S mbarriers (<= 32) + reduction banks
 constexpr int kMaxStages = 16;
-// W' (and the bias) live in registers; the shared-memory layout keeps a
-// slot for them (size 0 here) so the column store can move there.
-constexpr bool kStagedWReg = true;
+// Where a staged instantiation keeps W' (and the bias): registers up to 4
+// chunks per thread, shared memory beyond.
+__host__ __device__ constexpr bool staged_wreg(int npt) { return npt <= 4; }
 
 // Shared memory for per-column values (W', and the LayerNorm bias) when they
 // are kept in shared memory rather than registers.
@@ -65,10 +65,14 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
   constexpr int VEC = 16 / (int)sizeof(T);
   constexpr bool LN = (OP == LN_FWD || OP == LN_BWD);
   constexpr bool BWD = OpInfo<OP>::BWD;
-  constexpr bool WREG = kStagedWReg;             // W' (and bias) in registers
-  // LayerNorm and FusedAdd forwards keep their FP32 row in registers between
-  // passes; RMSNorm re-reads it from the stage (fewer registers, more CTAs).
-  constexpr bool KEEP = !BWD && OP != RMS_FWD;
+  // Up to 4 chunks per thread, W' (and the bias) live in registers; at 8
+  // (rows of 2049-4096 chunks) they move to shared memory to leave the
+  // registers to the dW / dB accumulators.
+  constexpr bool WREG = staged_wreg(NPT);
+  // The FusedAdd forward keeps its FP32 row h in registers between passes
+  // (up to 4 chunks per thread); RMSNorm and LayerNorm re-read theirs from
+  // the stage (fewer registers, more resident CTAs).
+  constexpr bool KEEP = (OP == FADD_FWD) && NPT <= 4;
   constexpr int NWR = WREG ? NPT : 1;
   constexpr int NB = (OP == LN_FWD && WREG) ? NPT : 1;   // bias registers
   constexpr int NDW = DW ? NPT : 1;
@@ -204,7 +208,8 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
         if constexpr (LN) mu_next = p.mean_in[row + G];
       }
     }
-    if (!mbar_wait_bounded(&bars[s], phase)) {
+    // (the LayerNorm forward waits for row k+1 during row k: see below)
+    if ((OP != LN_FWD || k == 0) && !mbar_wait_bounded(&bars[s], phase)) {
       atomicOr(p.status, STATUS_WAIT_TIMEOUT);
       abort_flag[fl] = 1;
     }
@@ -221,7 +226,104 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
       if (tid == 0 && !abort_flag[fl] && issued < nrows) issue_next();
     };
 
-    if constexpr (!BWD) {
+    if constexpr (OP == LN_FWD) {
+      // ---- LayerNorm forward, statistics software-pipelined -------------
+      // One barrier per row: it reduces the variance of row k (two-pass,
+      // about the mean found in the previous barrier) together with the sum
+      // of row k+1.  Rows k and k+1 are resident (the ring has >= 3 stages).
+      if (k == 0) {
+        float acc[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+#pragma unroll
+        for (int j = 0; j < NPT; ++j) {
+          const int c = tid + j * nt;
+          if (c < nchunks) {
+            float t[VEC];
+            P::unpack(r0[c], t);
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) acc[v] = fadd(acc[v], t[v]);
+          }
+        }
+        float a[1] = {tree_sum<VEC>(acc)};
+        block_sum<1>(a, red, bank);
+        after_first_barrier();
+        mu_next = div_n(a[0], inv_n);
+      }
+      mean = mu_next;
+      float xf[NX][VEC];
+      float accv[VEC], accs[VEC];
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) { accv[v] = 0.f; accs[v] = 0.f; }
+#pragma unroll
+      for (int j = 0; j < NPT; ++j) {
+        const int c = tid + j * nt;
+        float t[VEC];
+        if (c < nchunks) {
+          P::unpack(r0[c], t);
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) {
+            const float d = fsub(t[v], mean);
+            accv[v] = ffma(d, d, accv[v]);
+          }
+        } else {
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) t[v] = 0.f;
+        }
+        if constexpr (KEEP) {
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) xf[j][v] = t[v];
+        }
+      }
+      if (k + 1 < nrows) {
+        const int s1 = (s + 1 == S) ? 0 : s + 1;
+        const uint32_t ph1 = (s + 1 == S) ? (phase ^ 1u) : phase;
+        if (!mbar_wait_bounded(&bars[s1], ph1)) {
+          atomicOr(p.status, STATUS_WAIT_TIMEOUT);
+          abort_flag[fl] = 1;
+        }
+        const uint4* n0 = reinterpret_cast<const uint4*>(stages + (size_t)s1 * stage_bytes);
+#pragma unroll
+        for (int j = 0; j < NPT; ++j) {
+          const int c = tid + j * nt;
+          if (c < nchunks) {
+            float t[VEC];
+            P::unpack(n0[c], t);
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) accs[v] = fadd(accs[v], t[v]);
+          }
+        }
+      }
+      float a2[2] = {tree_sum<VEC>(accv), tree_sum<VEC>(accs)};
+      block_sum<2>(a2, red, bank);
+      after_first_barrier();
+      rstd = inv_rms(div_n(a2[0], inv_n), p.eps);
+      mu_next = div_n(a2[1], inv_n);
+      if (abort_flag[fl]) { aborted = true; break; }
+      if (tid == 0) {
+        if (p.rstd_out) p.rstd_out[row] = rstd;
+        if (p.mean_out) p.mean_out[row] = mean;
+      }
+      T* yrow = static_cast<T*>(p.out0) + row * p.s_out0;
+#pragma unroll
+      for (int j = 0; j < NPT; ++j) {
+        const int c = tid + j * nt;
+        if (c < nchunks) {
+          float t[VEC], w[VEC], bb[VEC], yf[VEC];
+          if constexpr (KEEP) {
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) t[v] = xf[j][v];
+          } else {
+            P::unpack(r0[c], t);
+          }
+          colv(j, c, 0, w);
+          colv(j, c, 1, bb);
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) yf[v] = ffma(fmul(fsub(t[v], mean), rstd), w[v], bb[v]);
+          st_global_cs16(yrow + (int64_t)c * VEC, P::pack(yf));
+        }
+      }
+    } else if constexpr (!BWD) {
       // ---- forward: the row (x, or h = x + residual) in FP32 -------------
       // row value of chunk c: x, or h = x + residual (FP32, exact for 16-bit
       // inputs); kept in registers (xf) or re-read from the stage
@@ -262,39 +364,9 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
       float a[1] = {tree_sum<VEC>(acc)};
       block_sum<1>(a, red, bank);
       after_first_barrier();
-      if constexpr (LN) {
-        mean = div_n(a[0], inv_n);
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
-#pragma unroll
-        for (int j = 0; j < NPT; ++j) {
-          const int c = tid + j * nt;
-          if (c < nchunks) {
-            float t[VEC];
-            if constexpr (KEEP) {
-#pragma unroll
-              for (int v = 0; v < VEC; ++v) t[v] = xf[j][v];
-            } else {
-              rowv(c, t);
-            }
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) {
-              const float d = fsub(t[v], mean);
-              acc[v] = ffma(d, d, acc[v]);
-            }
-          }
-        }
-        float q[1] = {tree_sum<VEC>(acc)};
-        block_sum<1>(q, red, bank);
-        rstd = inv_rms(div_n(q[0], inv_n), p.eps);
-      } else {
-        rstd = inv_rms(div_n(a[0], inv_n), p.eps);
-      }
+      rstd = inv_rms(div_n(a[0], inv_n), p.eps);
       if (abort_flag[fl]) { aborted = true; break; }
-      if (tid == 0) {
-        if (p.rstd_out) p.rstd_out[row] = rstd;
-        if (LN && p.mean_out) p.mean_out[row] = mean;
-      }
+      if (tid == 0 && p.rstd_out) p.rstd_out[row] = rstd;
       T* yrow = static_cast<T*>(p.out0) + row * p.s_out0;
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
@@ -308,15 +380,8 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
             rowv(c, t);
           }
           colv(j, c, 0, w);
-          if constexpr (OP == LN_FWD) {
-            float bb[VEC];
-            colv(j, c, 1, bb);
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) yf[v] = ffma(fmul(fsub(t[v], mean), rstd), w[v], bb[v]);
-          } else {
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) yf[v] = fmul(fmul(t[v], rstd), w[v]);
-          }
+          for (int v = 0; v < VEC; ++v) yf[v] = fmul(fmul(t[v], rstd), w[v]);
           st_global_cs16(yrow + (int64_t)c * VEC, P::pack(yf));
         }
       }
@@ -474,7 +539,7 @@ __global__ void __launch_bounds__(512) loop_kernel(const RowParams p) {
   constexpr int NR = (OP == LN_BWD) ? 2 : 1;
   const int N = p.N;
   const int tid = threadIdx.x, nt = blockDim.x;
-  __shared__ float red[2 * 32 * 2];
+  __shared__ float red[2 * 32 * kMaxReduceValues];
   int bank = 0;
   const TW* wp = static_cast<const TW*>(p.w);
   const TW* bp = static_cast<const TW*>(p.b);
@@ -657,8 +722,9 @@ int launch_staged(const RowParams& p, const DevInfo& di, int nin, int max_ctas, 
   const size_t stage_bytes = (size_t)nin * p.N * sizeof(T);
   auto fn = staged_kernel<OP, T, TW, NPT, DW, DB>;
   const void* fp = reinterpret_cast<const void*>(fn);
-  const size_t fixed = kStagedHeader + staged_col_bytes<OP>(p.N, kStagedWReg);
-  const size_t min_smem = fixed + 2 * stage_bytes;
+  const size_t fixed = kStagedHeader + staged_col_bytes<OP>(p.N, staged_wreg(NPT));
+  const int min_stages = (OP == LN_FWD) ? 3 : 2;   // the LayerNorm forward holds rows k and k+1
+  const size_t min_smem = fixed + (size_t)min_stages * stage_bytes;
   const int max_dyn = allow_max_smem(fp, di);
   if (max_dyn < 0) return NORM_ERR_CUDA;
   if (min_smem > (size_t)max_dyn) return NORM_ERR_UNSUPPORTED_INTERNAL;
@@ -677,17 +743,18 @@ int launch_staged(const RowParams& p, const DevInfo& di, int nin, int max_ctas, 
     if (per_cta < min_smem) continue;
     S = (int)((per_cta - fixed) / stage_bytes);
     if (S > kMaxStages) S = kMaxStages;
-    if (di.tune_max_stages >= 2 && S > di.tune_max_stages) S = di.tune_max_stages;
+    if (di.tune_max_stages >= 2 && S > di.tune_max_stages)
+      S = di.tune_max_stages > min_stages ? di.tune_max_stages : min_stages;
     // confirm `ctas` CTAs of this size are resident together
-    for (; S >= 2; --S) {
+    for (; S >= min_stages; --S) {
       smem = fixed + (size_t)S * stage_bytes;
       const int fit = cached_occupancy(fp, di, threads, smem);
       if (fit < 0) return NORM_ERR_CUDA;
       if (fit >= ctas) break;
     }
-    if (S >= 2) break;
+    if (S >= min_stages) break;
   }
-  if (ctas < 1 || S < 2) return NORM_ERR_UNSUPPORTED_INTERNAL;
+  if (ctas < 1 || S < min_stages) return NORM_ERR_UNSUPPORTED_INTERNAL;
   int64_t G = (int64_t)di.sms * ctas;
   if (G > p.M) G = p.M;
   if ((DW || DB) && G > di.max_partial_rows) G = di.max_partial_rows;
@@ -713,6 +780,8 @@ int launch_loop(const RowParams& p, const DevInfo& di, cudaStream_t st, int* gri
   return NORM_OK;
 }
 
+constexpr int kMaxStagedSpillBytes = 64;
+
 // How well one staged instantiation suits a shape: fits at all, spills
 // registers, CTAs resident per SM (at the two-stage minimum), block size.
 struct StagedFit {
@@ -730,10 +799,13 @@ StagedFit probe_staged(const RowParams& p, const DevInfo& di, int nin) {
   if (f.threads == 0) return f;
   const void* fp = reinterpret_cast<const void*>(staged_kernel<OP, T, TW, NPT, DW, DB>);
   const KernelInfo ki = kernel_info(fp, di);
-  const size_t min_smem = kStagedHeader + staged_col_bytes<OP>(p.N, kStagedWReg) + 2 * (size_t)nin * p.N * sizeof(T);
+  const size_t min_smem = kStagedHeader + staged_col_bytes<OP>(p.N, staged_wreg(NPT)) +
+                          (OP == LN_FWD ? 3 : 2) * (size_t)nin * p.N * sizeof(T);
   if (ki.max_dyn < 0 || min_smem > (size_t)ki.max_dyn) return f;
   const int nb = cached_occupancy(fp, di, f.threads, min_smem);
   if (nb <= 0) return f;
+  // a shape that spills more than a few registers loses to the general kernel
+  if (ki.local_bytes > kMaxStagedSpillBytes) return f;
   f.ok = true;
   f.spills = ki.local_bytes > 0;
   f.ctas = nb;
@@ -757,13 +829,14 @@ int launch_rows(const RowParams& p, const DevInfo& di, bool rows_aligned, cudaSt
     // reduction tree, so frozen and trainable calls give bit-identical dx.
     constexpr bool PDW = OpInfo<OP>::BWD;
     constexpr bool PDB = (OP == LN_BWD);
-    const StagedFit fits[3] = {probe_staged<OP, T, TW, 1, PDW, PDB>(p, di, nin),
+    const StagedFit fits[4] = {probe_staged<OP, T, TW, 1, PDW, PDB>(p, di, nin),
                                probe_staged<OP, T, TW, 2, PDW, PDB>(p, di, nin),
-                               probe_staged<OP, T, TW, 4, PDW, PDB>(p, di, nin)};
-    const int npts[3] = {1, 2, 4};
+                               probe_staged<OP, T, TW, 4, PDW, PDB>(p, di, nin),
+                               probe_staged<OP, T, TW, 8, PDW, PDB>(p, di, nin)};
+    const int npts[4] = {1, 2, 4, 8};
     int best = -1;
     long best_score = -1;
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < 4; ++i) {
       if (!fits[i].ok) continue;
       if (di.tune_npt && npts[i] != di.tune_npt) continue;
       const int d = fits[i].threads > 256 ? fits[i].threads - 256 : 256 - fits[i].threads;
@@ -775,6 +848,7 @@ int launch_rows(const RowParams& p, const DevInfo& di, bool rows_aligned, cudaSt
       case 1: rc = launch_staged<OP, T, TW, 1, DW, DB>(p, di, nin, max_ctas, st, grid_out); break;
       case 2: rc = launch_staged<OP, T, TW, 2, DW, DB>(p, di, nin, max_ctas, st, grid_out); break;
       case 4: rc = launch_staged<OP, T, TW, 4, DW, DB>(p, di, nin, max_ctas, st, grid_out); break;
+      case 8: rc = launch_staged<OP, T, TW, 8, DW, DB>(p, di, nin, max_ctas, st, grid_out); break;
       default: break;
     }
     if (rc != NORM_ERR_UNSUPPORTED_INTERNAL) return rc;

@@ -1,0 +1,268 @@
+"""Edge cases of the CUDA path, each against the FP64 oracle or against the
+same library's other route to the same result."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic_inputs as si
+from gpu_util import Strided, bits_equal, f64, workspace
+from test_parity_gpu import (EPS, check_fadd, check_ln, check_rms, run_fadd, run_ln, run_rms)
+from tolerance import check, check_dw, dtype_name, rounded
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def g():
+    from conftest import built_package
+    return built_package()
+
+
+@pytest.fixture
+def loop_path(g):
+    g.norm_debug_set_path(2)
+    yield
+    g.norm_debug_set_path(0)
+
+
+# ---------------------------------------------------------------------------
+# sizes
+# ---------------------------------------------------------------------------
+
+def test_zero_rows(g):
+    N = 64
+    x = torch.empty(0, N, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(N, dtype=torch.bfloat16, device="cuda")
+    g.norm_rms_fwd(x, w, torch.empty_like(x), torch.empty(0, device="cuda"))
+    dw = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+    g.norm_rms_bwd(x, x, w, torch.empty(0, device="cuda"), torch.empty_like(x), dw, None)
+    db = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+    dw2 = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+    g.norm_ln_bwd(x, x, w, None, None, torch.empty_like(x), dw2, db, None)
+    torch.cuda.synchronize()
+    assert bool((dw == 0).all()) and bool((dw2 == 0).all()) and bool((db == 0).all())
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 7, 8, 9, 33, 100, 129])
+@pytest.mark.parametrize("M", [1, 5])
+@pytest.mark.parametrize("dtype", ["bfloat16", "float32"])
+def test_tiny_rows(g, M, N, dtype):
+    case = si.norm_case(M, N, seed=N, dtype=dtype)
+    check_rms(run_rms(g, case), case, f"tiny rms {M}x{N} {dtype}")
+    if N > 1:   # a one-element row has zero variance: LayerNorm output is the bias
+        check_ln(run_ln(g, case), case, f"tiny ln {M}x{N} {dtype}")
+
+
+def test_single_element_layernorm_gives_bias(g):
+    case = si.norm_case(4, 1, seed=1, dtype="float32")
+    out = run_ln(g, case)
+    np.testing.assert_array_equal(out["y"].view.cpu().numpy()[:, 0], case["b"].numpy()[0])
+
+
+def test_wide_rows_general_kernel(g):
+    case = si.norm_case(3, 65537, seed=2, dtype="bfloat16")
+    check_rms(run_rms(g, case), case, "rms 3x65537")
+    check_ln(run_ln(g, case), case, "ln 3x65537")
+
+
+def test_many_narrow_rows(g):
+    case = si.norm_case(100000, 64, seed=3, dtype="bfloat16")
+    check_rms(run_rms(g, case), case, "rms 100000x64")
+    check_ln(run_ln(g, case), case, "ln 100000x64")
+
+
+# ---------------------------------------------------------------------------
+# alignment and kernel families
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("lead", [1, 2, 3, 5, 7])
+def test_unaligned_row_starts(g, lead):
+    case = si.norm_case(64, 4096, seed=lead, dtype="bfloat16", fused_add=True)
+    check_rms(run_rms(g, case, lead=lead), case, f"rms lead {lead}")
+    check_ln(run_ln(g, case, lead=lead), case, f"ln lead {lead}")
+
+
+@pytest.mark.parametrize("M,N", [(512, 4096), (256, 8192)])
+def test_general_kernel_matches_oracle_on_aligned_rows(g, loop_path, M, N):
+    case = si.norm_case(M, N, seed=4, dtype="bfloat16", fused_add=True)
+    check_rms(run_rms(g, case), case, "loop rms")
+    check_ln(run_ln(g, case), case, "loop ln")
+    check_fadd(run_fadd(g, case), case, "loop fadd")
+
+
+def test_kernel_families_agree(g):
+    case = si.norm_case(300, 8192, seed=5, dtype="bfloat16")
+    staged = run_rms(g, case)
+    g.norm_debug_set_path(2)
+    try:
+        loop = run_rms(g, case)
+    finally:
+        g.norm_debug_set_path(0)
+    a = staged["dx"].view.float()
+    b = loop["dx"].view.float()
+    # both round the same FP32 formula; they may differ by one bf16 ulp
+    assert float((a - b).abs().max()) <= float(a.abs().max()) * 2 ** -7
+    assert bits_equal(staged["y"].view, loop["y"].view) or \
+        float((staged["y"].view.float() - loop["y"].view.float()).abs().max()) <= 2 ** -6
+
+
+@pytest.mark.parametrize("dtype,wdtype", [("float16", "float32"), ("float32", "float32"), ("float16", "float16")])
+def test_other_dtypes_on_the_staged_kernel(g, dtype, wdtype):
+    case = si.norm_case(257, 8192, seed=6, dtype=dtype, w_dtype=wdtype, fused_add=True)
+    check_rms(run_rms(g, case), case, f"rms {dtype}/{wdtype}")
+    check_ln(run_ln(g, case), case, f"ln {dtype}/{wdtype}")
+    check_fadd(run_fadd(g, case), case, f"fadd {dtype}/{wdtype}")
+
+
+# ---------------------------------------------------------------------------
+# in place and recomputed statistics
+# ---------------------------------------------------------------------------
+
+def test_in_place_calls_match_out_of_place(g):
+    M, N = 333, 8192
+    case = si.norm_case(M, N, seed=7, dtype="bfloat16", fused_add=True)
+    d = {k: v.cuda() for k, v in case.items()}
+    rstd = torch.empty(M, device="cuda")
+    # RMSNorm forward, y == x
+    y = torch.empty_like(d["x"])
+    g.norm_rms_fwd(d["x"], d["w"], y, rstd)
+    xi = d["x"].clone()
+    g.norm_rms_fwd(xi, d["w"], xi, rstd)
+    assert bits_equal(xi, y)
+    # LayerNorm forward, y == x
+    mean = torch.empty(M, device="cuda")
+    g.norm_ln_fwd(d["x"], d["w"], d["b"], y, mean, rstd)
+    xi = d["x"].clone()
+    g.norm_ln_fwd(xi, d["w"], d["b"], xi, mean, rstd)
+    assert bits_equal(xi, y)
+    # RMSNorm backward, dx == dy
+    g.norm_rms_fwd(d["x"], d["w"], y, rstd)
+    dx = torch.empty_like(d["x"])
+    g.norm_rms_bwd(d["dy"], d["x"], d["w"], rstd, dx)
+    dyi = d["dy"].clone()
+    g.norm_rms_bwd(dyi, d["x"], d["w"], rstd, dyi)
+    assert bits_equal(dyi, dx)
+    # FusedAdd forward, h_out == residual; backward, dx == dh_out
+    h = torch.empty_like(d["x"])
+    g.norm_fused_add_rms_fwd(d["x"], d["residual"], d["w"], y, h, rstd)
+    ri = d["residual"].clone()
+    y2 = torch.empty_like(y)
+    g.norm_fused_add_rms_fwd(d["x"], ri, d["w"], y2, ri, rstd)
+    assert bits_equal(ri, h) and bits_equal(y2, y)
+    g.norm_fused_add_rms_bwd(d["dy"], d["dh_out"], h, d["w"], rstd, dx)
+    dhi = d["dh_out"].clone()
+    g.norm_fused_add_rms_bwd(d["dy"], dhi, h, d["w"], rstd, dhi)
+    torch.cuda.synchronize()
+    assert bits_equal(dhi, dx)
+
+
+@pytest.mark.parametrize("N", [4096, 4095])
+def test_backward_recomputes_statistics(g, N):
+    M = 200
+    case = si.norm_case(M, N, seed=8, dtype="bfloat16")
+    x, dy, w = (case[k].cuda() for k in ("x", "dy", "w"))
+    x64, dy64, w64 = f64(case["x"]), f64(case["dy"]), f64(case["w"])
+    dx = torch.empty_like(x)
+    g.norm_rms_bwd(dy, x, w, None, dx)
+    ref, _, sc = oracle.rms_bwd(x64, dy64, w64, 0.0, EPS, with_scale=True)
+    check(dx, ref, "bfloat16", scale=sc, label="rms bwd recomputed rstd")
+    g.norm_ln_bwd(dy, x, w, None, None, dx)
+    ref, _, _, sc = oracle.ln_bwd(x64, dy64, w64, 0.0, EPS, with_scale=True)
+    torch.cuda.synchronize()
+    check(dx, ref, "bfloat16", scale=sc, label="ln bwd recomputed stats")
+
+
+# ---------------------------------------------------------------------------
+# determinism, streams, graphs
+# ---------------------------------------------------------------------------
+
+def test_weight_gradients_are_deterministic(g):
+    M, N = 4096, 8192
+    case = si.norm_case(M, N, seed=9, dtype="bfloat16")
+    a = run_ln(g, case, dw_dtype=torch.float32)
+    b = run_ln(g, case, dw_dtype=torch.float32)
+    assert bits_equal(a["dw"], b["dw"]) and bits_equal(a["db"], b["db"])
+    c = run_rms(g, case, dw_dtype=torch.float32)
+    e = run_rms(g, case, dw_dtype=torch.float32)
+    assert bits_equal(c["dw"], e["dw"])
+
+
+def test_non_default_stream(g):
+    M, N = 1024, 4096
+    case = si.norm_case(M, N, seed=10, dtype="bfloat16")
+    x, dy, w = (case[k].cuda() for k in ("x", "dy", "w"))
+    s = torch.cuda.Stream()
+    y, dx = torch.empty_like(x), torch.empty_like(x)
+    rstd = torch.empty(M, device="cuda")
+    dw = torch.empty(N, dtype=torch.float32, device="cuda")
+    ws = workspace(g, M, N, True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        g.norm_rms_fwd(x, w, y, rstd)
+        g.norm_rms_bwd(dy, x, w, rstd, dx, dw, ws)
+    s.synchronize()
+    ref_y, _ = oracle.rms_fwd(f64(case["x"]), f64(case["w"]), 0.0, EPS)
+    check(y, ref_y, "bfloat16", label="stream y")
+    ref_dx, ref_dw, sc = oracle.rms_bwd(f64(case["x"]), f64(case["dy"]), f64(case["w"]), 0.0, EPS,
+                                        with_scale=True)
+    check(dx, ref_dx, "bfloat16", scale=sc, label="stream dx")
+
+
+def test_cuda_graph_replay_with_changed_inputs(g):
+    """Capture forward + trainable backward once, then replay after writing
+    new x, w and dy into the captured buffers ([B] diagnostics: CUDA Graph
+    replay with changed X, W and dY)."""
+    M, N = 2048, 4096
+    cases = [si.norm_case(M, N, seed=s, dtype="bfloat16", gemma=True, with_bias=False) for s in (20, 21)]
+    x = cases[0]["x"].cuda()
+    dy = cases[0]["dy"].cuda()
+    w = cases[0]["w"].cuda()
+    y, dx = torch.empty_like(x), torch.empty_like(x)
+    rstd = torch.empty(M, device="cuda")
+    dw = torch.empty(N, dtype=torch.float32, device="cuda")
+    ws = workspace(g, M, N, True)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):      # warm-up outside capture (first-use setup)
+        g.norm_rms_fwd(x, w, y, rstd, 1.0)
+        g.norm_rms_bwd(dy, x, w, rstd, dx, dw, ws, 1.0)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        g.norm_rms_fwd(x, w, y, rstd, 1.0)
+        g.norm_rms_bwd(dy, x, w, rstd, dx, dw, ws, 1.0)
+    for case in cases[::-1] + cases:
+        x.copy_(case["x"])
+        dy.copy_(case["dy"])
+        w.copy_(case["w"])
+        graph.replay()
+        torch.cuda.synchronize()
+        x64, dy64, w64 = f64(case["x"]), f64(case["dy"]), f64(case["w"])
+        ry, rr = oracle.rms_fwd(x64, w64, 1.0, EPS)
+        rdx, rdw, sc = oracle.rms_bwd(x64, dy64, w64, 1.0, EPS, with_scale=True, rstd=rr)
+        check(y, ry, "bfloat16", label="graph y")
+        check(dx, rdx, "bfloat16", scale=sc, label="graph dx")
+        xh = oracle.rms_fwd(x64, np.ones(N), 0.0, EPS)[0]
+        check_dw(dw, rdw, "float32", np.abs(dy64 * xh).sum(0), label="graph dw")
+
+
+# ---------------------------------------------------------------------------
+# errors that need the device's size
+# ---------------------------------------------------------------------------
+
+def test_workspace_one_byte_short_is_refused(g):
+    M, N = 1024, 4096
+    x = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(N, dtype=torch.bfloat16, device="cuda")
+    nb = g.norm_bwd_workspace_bytes(M, N, True)
+    assert nb > 0 and g.norm_bwd_workspace_bytes(M, N, False, False) == 0
+    ws = torch.empty(nb - 1, dtype=torch.uint8, device="cuda")
+    with pytest.raises(g.NormError) as e:
+        g.norm_rms_bwd(x, x, w, None, torch.empty_like(x), torch.empty(N, device="cuda"), ws)
+    assert e.value.status == 5
+
+
+def test_device_status_is_clear(g):
+    assert g.norm_device_status(reset=False) == 0

