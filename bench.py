@@ -518,16 +518,30 @@ def shape_table(g, flush_l2, reps=40):
     return rows
 
 
+def kernel_source_hash():
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "row_normalization_rmsnorm_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def load_profile_traffic(op, M, N):
-    """dram bytes per call of the operation's kernels from the committed ncu
-    summary, if one exists for this exact workload; else None."""
+    """DRAM bytes (read + write) per call of the operation's kernels, from the
+    committed ncu capture of this exact workload -- or None when there is
+    none, or when the kernel sources changed since it was taken."""
     path = os.path.join(ROOT, "profiles", f"ncu_traffic_{M}x{N}.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return d.get(op)
     except (OSError, ValueError):
         return None
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    t = d.get("traffic", {}).get(op)
+    return None if t is None else t.get("per_call")
 
 
 def run_e2e(wl, stream, steps, M, N, ops):
