@@ -1,0 +1,183 @@
+"""torch.autograd Functions and nn.Modules over the C ABI.
+
+The frozen-parameter rule of "perf(norm): skip dW/dB calculation when
+parameters are frozen" (Key Changes): each backward asks
+``ctx.needs_input_grad`` whether the weight (and the LayerNorm bias) need a
+gradient and passes NULL for those that do not, so a frozen parameter gets
+no workspace, no partial sums and no column reduction, only dx.  A call in
+which nothing requires grad saves nothing for a backward.
+
+All arithmetic runs in the library's kernels; this module allocates the
+outputs (and the dW / dB workspace) with torch and marshals arguments.
+Inputs may have any leading shape; the last dimension is normalised and
+must be contiguous.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _binding as B
+
+
+def _rows(t: torch.Tensor) -> torch.Tensor:
+    """A 2-D [rows, N] view with contiguous rows (copying only if needed)."""
+    if t.dim() == 0:
+        raise ValueError("expected at least one dimension")
+    if t.stride(-1) != 1:
+        t = t.contiguous()
+    try:
+        return t.view(-1, t.shape[-1])
+    except RuntimeError:
+        return t.contiguous().view(-1, t.shape[-1])
+
+
+def _workspace(M, N, dw, db, device):
+    nb = B.norm_bwd_workspace_bytes(M, N, dw, db)
+    return torch.empty(nb, dtype=torch.uint8, device=device) if nb else None
+
+
+class RMSNormFunction(torch.autograd.Function):
+    """y = x * rstd * (w + offset), rstd = 1/sqrt(mean(x^2) + eps)."""
+
+    @staticmethod
+    def forward(ctx, x, w, eps=1e-6, offset=0.0):
+        x2 = _rows(x)
+        M, N = x2.shape
+        y = torch.empty_like(x2)
+        rstd = torch.empty(M, dtype=torch.float32, device=x.device)
+        B.norm_rms_fwd(x2, w, y, rstd, offset, eps)
+        ctx.eps, ctx.offset = eps, offset
+        ctx.save_for_backward(x2, w, rstd)
+        return y.view(x.shape)
+
+    @staticmethod
+    def backward(ctx, dy):
+        x2, w, rstd = ctx.saved_tensors
+        need_dx, need_dw = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
+        if not (need_dx or need_dw):
+            return None, None, None, None
+        M, N = x2.shape
+        dy2 = _rows(dy)
+        dx = torch.empty_like(x2)
+        dw = torch.empty_like(w) if need_dw else None
+        B.norm_rms_bwd(dy2, x2, w, rstd, dx, dw, _workspace(M, N, need_dw, False, x2.device) if need_dw else None,
+                       ctx.offset, ctx.eps)
+        return (dx.view(dy.shape) if need_dx else None), dw, None, None
+
+
+class LayerNormFunction(torch.autograd.Function):
+    """y = (x - mean) * rstd * (w + offset) + b (b may be None)."""
+
+    @staticmethod
+    def forward(ctx, x, w, b=None, eps=1e-6, offset=0.0):
+        x2 = _rows(x)
+        M, N = x2.shape
+        y = torch.empty_like(x2)
+        mean = torch.empty(M, dtype=torch.float32, device=x.device)
+        rstd = torch.empty(M, dtype=torch.float32, device=x.device)
+        B.norm_ln_fwd(x2, w, b, y, mean, rstd, offset, eps)
+        ctx.eps, ctx.offset = eps, offset
+        ctx.has_b = b is not None
+        ctx.save_for_backward(x2, w, mean, rstd)
+        return y.view(x.shape)
+
+    @staticmethod
+    def backward(ctx, dy):
+        x2, w, mean, rstd = ctx.saved_tensors
+        need_dx, need_dw = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
+        need_db = ctx.has_b and ctx.needs_input_grad[2]
+        if not (need_dx or need_dw or need_db):
+            return None, None, None, None, None
+        M, N = x2.shape
+        dy2 = _rows(dy)
+        dx = torch.empty_like(x2)
+        dw = torch.empty_like(w) if need_dw else None
+        db = torch.empty_like(w) if need_db else None
+        ws = _workspace(M, N, need_dw, need_db, x2.device) if (need_dw or need_db) else None
+        B.norm_ln_bwd(dy2, x2, w, mean, rstd, dx, dw, db, ws, ctx.offset, ctx.eps)
+        return (dx.view(dy.shape) if need_dx else None), dw, db, None, None
+
+
+class FusedAddRMSNormFunction(torch.autograd.Function):
+    """h = x + residual; y = RMSNorm(h) * (w + offset).  Returns (y, h)."""
+
+    @staticmethod
+    def forward(ctx, x, residual, w, eps=1e-6, offset=0.0):
+        x2, r2 = _rows(x), _rows(residual)
+        M, N = x2.shape
+        y = torch.empty_like(x2)
+        h = torch.empty_like(x2)
+        rstd = torch.empty(M, dtype=torch.float32, device=x.device)
+        B.norm_fused_add_rms_fwd(x2, r2, w, y, h, rstd, offset, eps)
+        ctx.eps, ctx.offset = eps, offset
+        ctx.save_for_backward(h, w, rstd)
+        return y.view(x.shape), h.view(x.shape)
+
+    @staticmethod
+    def backward(ctx, dy, dh):
+        h, w, rstd = ctx.saved_tensors
+        need_x, need_r, need_dw = ctx.needs_input_grad[0], ctx.needs_input_grad[1], ctx.needs_input_grad[2]
+        if not (need_x or need_r or need_dw):
+            return None, None, None, None, None
+        M, N = h.shape
+        if dy is None:
+            dy = torch.zeros_like(h)
+        dy2 = _rows(dy)
+        dh2 = None if dh is None else _rows(dh)
+        dx = torch.empty_like(h)
+        dw = torch.empty_like(w) if need_dw else None
+        B.norm_fused_add_rms_bwd(dy2, dh2, h, w, rstd, dx, dw,
+                                 _workspace(M, N, need_dw, False, h.device) if need_dw else None, ctx.offset, ctx.eps)
+        # h = x + residual: one gradient serves both inputs
+        g = dx.view(dy.shape)
+        return (g if need_x else None), (g if need_r else None), dw, None, None
+
+
+def rms_norm(x, weight, eps=1e-6, offset=0.0):
+    return RMSNormFunction.apply(x, weight, eps, offset)
+
+
+def layer_norm(x, weight, bias=None, eps=1e-6, offset=0.0):
+    return LayerNormFunction.apply(x, weight, bias, eps, offset)
+
+
+def fused_add_rms_norm(x, residual, weight, eps=1e-6, offset=0.0):
+    return FusedAddRMSNormFunction.apply(x, residual, weight, eps, offset)
+
+
+class RMSNorm(torch.nn.Module):
+    """RMSNorm over the last dimension; offset=1 with zero-initialised weight
+    is the Gemma form y = x * rstd * (1 + w)."""
+
+    def __init__(self, hidden, eps=1e-6, offset=0.0, dtype=torch.bfloat16, device="cuda"):
+        super().__init__()
+        init = torch.zeros if offset else torch.ones
+        self.weight = torch.nn.Parameter(init(hidden, dtype=dtype, device=device))
+        self.eps, self.offset = eps, offset
+
+    def forward(self, x):
+        return rms_norm(x, self.weight, self.eps, self.offset)
+
+
+class LayerNorm(torch.nn.Module):
+    def __init__(self, hidden, eps=1e-6, bias=True, dtype=torch.bfloat16, device="cuda"):
+        super().__init__()
+        self.weight = torch.nn.Parameter(torch.ones(hidden, dtype=dtype, device=device))
+        self.bias = torch.nn.Parameter(torch.zeros(hidden, dtype=dtype, device=device)) if bias else None
+        self.eps = eps
+
+    def forward(self, x):
+        return layer_norm(x, self.weight, self.bias, self.eps)
+
+
+class FusedAddRMSNorm(torch.nn.Module):
+    """Returns (normalised, residual stream) for h = x + residual."""
+
+    def __init__(self, hidden, eps=1e-6, offset=0.0, dtype=torch.bfloat16, device="cuda"):
+        super().__init__()
+        init = torch.zeros if offset else torch.ones
+        self.weight = torch.nn.Parameter(init(hidden, dtype=dtype, device=device))
+        self.eps, self.offset = eps, offset
+
+    def forward(self, x, residual):
+        return fused_add_rms_norm(x, residual, self.weight, self.eps, self.offset)

@@ -2,7 +2,7 @@
 //
 // The row kernels leave one FP32 partial row per CTA ([G][N]).  Each CTA of
 // this kernel owns 32 adjacent columns: its 8 warps sum interleaved subsets of
-// the partial rows (warp k takes rows k, k+8, ..., in four independent
+// the partial rows (warp k takes rows k, k+8, ..., in eight independent
 // chains), coalesced 128-byte row segments, and warp 0 adds the 8 subtotals
 // in order.  The order of every
 // addition is fixed by (G, N), so dW / dB are bit-identical from run to run.
@@ -20,18 +20,29 @@ __global__ void __launch_bounds__(256) colreduce_kernel(const float* __restrict_
   const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
   const int col = blockIdx.x * 32 + lane;
   __shared__ float part[8][33];
-  // four independent chains per thread (rows grp, grp+8, grp+16, grp+24 of
-  // each block of 32), joined in a fixed order
-  float a[4] = {0.f, 0.f, 0.f, 0.f};
+  // The partial rows are written by the row kernel launched just before on
+  // the same stream; with programmatic dependent launch this kernel may
+  // start early, so it waits here until that grid has completed and its
+  // writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // eight independent chains per thread (rows grp + 8u, u < 8, of each
+  // block of 64 rows), joined in a fixed order
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (col < N) {
     int g = grp;
-    for (; g + 24 < G; g += 32) {
+    for (; g + 56 < G; g += 64) {
+      float t[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) a[u] = fadd(a[u], ws[(int64_t)(g + 8 * u) * N + col]);
+      for (int u = 0; u < 8; ++u) t[u] = ws[(int64_t)(g + 8 * u) * N + col];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) a[u] = fadd(a[u], t[u]);
     }
-    for (int u = 0; g < G; g += 8, ++u) a[u] = fadd(a[u], ws[(int64_t)g * N + col]);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (g + 8 * u < G) a[u] = fadd(a[u], ws[(int64_t)(g + 8 * u) * N + col]);
+    }
   }
-  const float acc = fadd(fadd(a[0], a[1]), fadd(a[2], a[3]));
+  const float acc = fadd(fadd(fadd(a[0], a[1]), fadd(a[2], a[3])), fadd(fadd(a[4], a[5]), fadd(a[6], a[7])));
   part[grp][lane] = acc;
   __syncthreads();
   if (grp == 0 && col < N) {
@@ -42,11 +53,24 @@ __global__ void __launch_bounds__(256) colreduce_kernel(const float* __restrict_
   }
 }
 
+// Launched with programmatic stream serialisation: the grid may be scheduled
+// while the row kernel before it drains (it signals once each of its CTAs
+// has finished its rows), and waits in-kernel for that grid's completion.
 template <class TO>
 static int launch_cr(const float* a, void* da, const float* b, void* db, int G, int N, cudaStream_t st) {
-  dim3 grid((unsigned)((N + 31) / 32), db ? 2u : 1u);
-  colreduce_kernel<TO><<<grid, 256, 0, st>>>(a, static_cast<TO*>(da), b, static_cast<TO*>(db), G, N);
-  return launch_status();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((N + 31) / 32), db ? 2u : 1u);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, colreduce_kernel<TO>, a, static_cast<TO*>(da), b,
+                                           static_cast<TO*>(db), G, N);
+  return e == cudaSuccess ? NORM_OK : cuda_fail(e);
 }
 
 int launch_colreduce(const float* ws_dw, void* dw, const float* ws_db, void* db, int G, int N, int out_dtype,

@@ -512,6 +512,9 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
   }
 
   if constexpr (DW || DB) {
+    // let the column reduce that follows be scheduled while this grid drains
+    // (it waits for the grid's completion before reading the partials)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #pragma unroll
     for (int j = 0; j < NPT; ++j) {
       const int c = tid + j * nt;
@@ -648,6 +651,7 @@ __global__ void __launch_bounds__(512) loop_kernel(const RowParams p) {
     }
     first = false;
   }
+  if constexpr (DW || DB) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ===========================================================================
