@@ -21,10 +21,10 @@ __global__ void __launch_bounds__(256) colreduce_kernel(const float* __restrict_
   const int col = blockIdx.x * 32 + lane;
   __shared__ float part[8][33];
   // The partial rows are written by the row kernel launched just before on
-  // the same stream; with programmatic dependent launch this kernel may
-  // start early, so it waits here until that grid has completed and its
-  // writes are visible.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the same stream; this kernel may start while that grid drains, so it
+  // waits here until the grid has completed and its writes are visible.
+  grid_dependency_wait();
+  grid_launch_dependents();
   // eight independent chains per thread (rows grp + 8u, u < 8, of each
   // block of 64 rows), joined in a fixed order
   float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -53,24 +53,10 @@ __global__ void __launch_bounds__(256) colreduce_kernel(const float* __restrict_
   }
 }
 
-// Launched with programmatic stream serialisation: the grid may be scheduled
-// while the row kernel before it drains (it signals once each of its CTAs
-// has finished its rows), and waits in-kernel for that grid's completion.
 template <class TO>
 static int launch_cr(const float* a, void* da, const float* b, void* db, int G, int N, cudaStream_t st) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((N + 31) / 32), db ? 2u : 1u);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, colreduce_kernel<TO>, a, static_cast<TO*>(da), b,
-                                           static_cast<TO*>(db), G, N);
-  return e == cudaSuccess ? NORM_OK : cuda_fail(e);
+  return launch_pdl(colreduce_kernel<TO>, dim3((unsigned)((N + 31) / 32), db ? 2u : 1u), dim3(256), 0, st, a,
+                    static_cast<TO*>(da), b, static_cast<TO*>(db), G, N);
 }
 
 int launch_colreduce(const float* ws_dw, void* dw, const float* ws_db, void* db, int G, int N, int out_dtype,

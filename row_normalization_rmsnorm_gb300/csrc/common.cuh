@@ -259,6 +259,17 @@ __device__ __forceinline__ void st_global_cs16(void* p, uint4 v) {
                : "memory");
 }
 
+// Programmatic dependent launch.  Every kernel of this library is launched
+// so that it may start while the previous kernel on the stream drains; it
+// calls grid_dependency_wait() before its first global-memory access (which
+// returns once the previous grid has completed and its writes are visible,
+// at once when there is no such grid), and grid_launch_dependents() once its
+// own main work is done, letting the next kernel be scheduled early.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Status bits written to RowParams::status.
 enum : int { STATUS_WAIT_TIMEOUT = 1 };
 

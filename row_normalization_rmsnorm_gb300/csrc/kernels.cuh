@@ -97,6 +97,8 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
   // the others read for row k.
   __shared__ int abort_flag[2];
 
+  grid_dependency_wait();
+
   // Per-thread constant columns: W' = float(w) + offset (and the LayerNorm
   // bias) in FP32, formed once per CTA.
   float wv[NWR][VEC];
@@ -499,6 +501,7 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
     }
   }
 
+  grid_launch_dependents();
   if (aborted) {
     // Bounded drain of the copies still in flight into this CTA's shared
     // memory (rows k .. issued-1), then leave without writing partial sums.
@@ -512,9 +515,6 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
   }
 
   if constexpr (DW || DB) {
-    // let the column reduce that follows be scheduled while this grid drains
-    // (it waits for the grid's completion before reading the partials)
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #pragma unroll
     for (int j = 0; j < NPT; ++j) {
       const int c = tid + j * nt;
@@ -547,6 +547,7 @@ __global__ void __launch_bounds__(512) loop_kernel(const RowParams p) {
   const TW* wp = static_cast<const TW*>(p.w);
   const TW* bp = static_cast<const TW*>(p.b);
   const float inv_n = 1.0f / (float)N;
+  grid_dependency_wait();
   float* wsw = nullptr;
   float* wsb = nullptr;
   if constexpr (DW) wsw = p.ws_dw + (int64_t)blockIdx.x * N;
@@ -651,7 +652,7 @@ __global__ void __launch_bounds__(512) loop_kernel(const RowParams p) {
     }
     first = false;
   }
-  if constexpr (DW || DB) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  grid_launch_dependents();
 }
 
 // ===========================================================================
@@ -762,8 +763,7 @@ int launch_staged(const RowParams& p, const DevInfo& di, int nin, int max_ctas, 
   int64_t G = (int64_t)di.sms * ctas;
   if (G > p.M) G = p.M;
   if ((DW || DB) && G > di.max_partial_rows) G = di.max_partial_rows;
-  fn<<<(unsigned)G, threads, smem, st>>>(p, S);
-  if (launch_status() != NORM_OK) return NORM_ERR_CUDA;
+  if (launch_pdl(fn, dim3((unsigned)G), dim3(threads), smem, st, p, S) != NORM_OK) return NORM_ERR_CUDA;
   *grid_out = (int)G;
   return NORM_OK;
 }
@@ -778,8 +778,7 @@ int launch_loop(const RowParams& p, const DevInfo& di, cudaStream_t st, int* gri
   int64_t G = (int64_t)di.sms * nb;
   if (G > p.M) G = p.M;
   if ((DW || DB) && G > di.max_partial_rows) G = di.max_partial_rows;
-  fn<<<(unsigned)G, threads, 0, st>>>(p);
-  if (launch_status() != NORM_OK) return NORM_ERR_CUDA;
+  if (launch_pdl(fn, dim3((unsigned)G), dim3(threads), 0, st, p) != NORM_OK) return NORM_ERR_CUDA;
   *grid_out = (int)G;
   return NORM_OK;
 }

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/gb300norm.h"
 #include "common.cuh"
 
@@ -19,6 +21,24 @@ int cuda_fail(cudaError_t e);
 // Launch status of the kernel just enqueued: NORM_OK or NORM_ERR_CUDA.
 inline int launch_status() {
   const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? NORM_OK : cuda_fail(e);
+}
+
+// Launch `kernel` on `st` with programmatic stream serialisation (see
+// grid_dependency_wait in common.cuh).  NORM_OK or NORM_ERR_CUDA.
+template <class... KArgs, class... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
   return e == cudaSuccess ? NORM_OK : cuda_fail(e);
 }
 
