@@ -784,6 +784,7 @@ int launch_loop(const RowParams& p, const DevInfo& di, cudaStream_t st, int* gri
 }
 
 constexpr int kMaxStagedSpillBytes = 64;
+constexpr int kTinySpillBytes = 32;   // a spill this small counts as none
 
 // How well one staged instantiation suits a shape: fits at all, spills
 // registers, CTAs resident per SM (at the two-stage minimum), block size.
@@ -810,7 +811,7 @@ StagedFit probe_staged(const RowParams& p, const DevInfo& di, int nin) {
   // a shape that spills more than a few registers loses to the general kernel
   if (ki.local_bytes > kMaxStagedSpillBytes) return f;
   f.ok = true;
-  f.spills = ki.local_bytes > 0;
+  f.spills = ki.local_bytes > kTinySpillBytes;
   f.ctas = nb;
   return f;
 }
@@ -818,8 +819,9 @@ StagedFit probe_staged(const RowParams& p, const DevInfo& di, int nin) {
 // Row kernel for one (op, types, flags): the staged path when every streamed
 // row starts on a 16-byte boundary and fits, else the loop path.  Among the
 // staged shapes (1, 2 or 4 chunks per thread) the choice prefers, in order:
-// no register spills, at least two resident CTAs per SM (so one CTA's
-// barrier overlaps another's work), and blocks of about 256 threads.
+// no register spills (a few bytes aside), at least two resident CTAs per SM
+// (so one CTA's barrier overlaps another's work), and blocks of about 256
+// threads.
 template <int OP, class T, class TW, bool DW, bool DB>
 int launch_rows(const RowParams& p, const DevInfo& di, bool rows_aligned, cudaStream_t st, int* grid_out) {
   constexpr int VEC = 16 / (int)sizeof(T);
