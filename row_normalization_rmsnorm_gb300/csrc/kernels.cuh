@@ -99,6 +99,42 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
 
   grid_dependency_wait();
 
+  const int64_t G = gridDim.x;
+  const int64_t row0 = blockIdx.x;
+  const int64_t nrows = (p.M - row0 + G - 1) / G;   // >= 1: the grid never exceeds M
+  const uint64_t pol = l2_policy_evict_first();
+  const char* g0 = static_cast<const char*>(p.in0);
+  const char* g1 = static_cast<const char*>(p.in1);
+  const char* g2 = static_cast<const char*>(p.in2);
+  const float inv_n = 1.0f / (float)N;
+  // Producer state (thread 0): rows of this CTA whose copies have been
+  // issued, and the stage the next one goes to.  Stage and phase indices
+  // advance by counting, never by dividing the row index.
+  int64_t issued = 0;
+  int istage = 0;
+
+  auto issue_next = [&]() {
+    const int64_t row = row0 + issued * G;
+    unsigned char* dst = stages + (size_t)istage * stage_bytes;
+    uint64_t* bar = &bars[istage];
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar, stage_bytes);
+    bulk_g2s(dst, g0 + row * p.s_in0 * (int64_t)sizeof(T), row_bytes, bar, pol);
+    if (nin > 1) bulk_g2s(dst + row_bytes, g1 + row * p.s_in1 * (int64_t)sizeof(T), row_bytes, bar, pol);
+    if (nin > 2) bulk_g2s(dst + 2 * row_bytes, g2 + row * p.s_in2 * (int64_t)sizeof(T), row_bytes, bar, pol);
+    ++issued;
+    if (++istage == S) istage = 0;
+  };
+  // Thread 0 sets up the ring and issues the first S-1 row copies before the
+  // per-column values are loaded, so the two latencies overlap.
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+    abort_flag[0] = 0;
+    abort_flag[1] = 0;
+    while (issued < nrows && issued < S - 1) issue_next();
+  }
+
   // Per-thread constant columns: W' = float(w) + offset (and the LayerNorm
   // bias) in FP32, formed once per CTA.
   float wv[NWR][VEC];
@@ -146,43 +182,8 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
 #pragma unroll
     for (int v = 0; v < VEC; ++v) dba[j][v] = 0.f;
 
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
-    fence_mbar_init();
-    abort_flag[0] = 0;
-    abort_flag[1] = 0;
-  }
-  __syncthreads();
+  __syncthreads();   // ring initialised (and first copies issued) by thread 0
 
-  const int64_t G = gridDim.x;
-  const int64_t row0 = blockIdx.x;
-  const int64_t nrows = (p.M - row0 + G - 1) / G;   // >= 1: the grid never exceeds M
-  const uint64_t pol = l2_policy_evict_first();
-  const char* g0 = static_cast<const char*>(p.in0);
-  const char* g1 = static_cast<const char*>(p.in1);
-  const char* g2 = static_cast<const char*>(p.in2);
-  const float inv_n = 1.0f / (float)N;
-  // Producer state (thread 0): rows of this CTA whose copies have been
-  // issued, and the stage the next one goes to.  Stage and phase indices
-  // advance by counting, never by dividing the row index.
-  int64_t issued = 0;
-  int istage = 0;
-
-  auto issue_next = [&]() {
-    const int64_t row = row0 + issued * G;
-    unsigned char* dst = stages + (size_t)istage * stage_bytes;
-    uint64_t* bar = &bars[istage];
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, stage_bytes);
-    bulk_g2s(dst, g0 + row * p.s_in0 * (int64_t)sizeof(T), row_bytes, bar, pol);
-    if (nin > 1) bulk_g2s(dst + row_bytes, g1 + row * p.s_in1 * (int64_t)sizeof(T), row_bytes, bar, pol);
-    if (nin > 2) bulk_g2s(dst + 2 * row_bytes, g2 + row * p.s_in2 * (int64_t)sizeof(T), row_bytes, bar, pol);
-    ++issued;
-    if (++istage == S) istage = 0;
-  };
-  if (tid == 0) {
-    while (issued < nrows && issued < S - 1) issue_next();
-  }
 
   // Saved statistics of the backward are read one row ahead, off the
   // critical path of the row being processed.
