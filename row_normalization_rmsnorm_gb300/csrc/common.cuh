@@ -77,6 +77,13 @@ template <> struct Pack16<float> {
   static __device__ __forceinline__ uint4 pack(const float (&f)[4]) {
     return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
   }
+  static __device__ __forceinline__ void unpack(const uint4& u, float2 (&f)[2]) {
+    f[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+    f[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+  }
+  static __device__ __forceinline__ uint4 pack(const float2 (&f)[2]) {
+    return make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y), __float_as_uint(f[1].x), __float_as_uint(f[1].y));
+  }
 };
 template <> struct Pack16<__nv_bfloat16> {
   static __device__ __forceinline__ void word(uint32_t w, float& lo, float& hi) {
@@ -92,6 +99,12 @@ template <> struct Pack16<__nv_bfloat16> {
   }
   static __device__ __forceinline__ uint4 pack(const float (&f)[8]) {
     return make_uint4(two(f[0], f[1]), two(f[2], f[3]), two(f[4], f[5]), two(f[6], f[7]));
+  }
+  static __device__ __forceinline__ void unpack(const uint4& u, float2 (&f)[4]) {
+    word(u.x, f[0].x, f[0].y); word(u.y, f[1].x, f[1].y); word(u.z, f[2].x, f[2].y); word(u.w, f[3].x, f[3].y);
+  }
+  static __device__ __forceinline__ uint4 pack(const float2 (&f)[4]) {
+    return make_uint4(two(f[0].x, f[0].y), two(f[1].x, f[1].y), two(f[2].x, f[2].y), two(f[3].x, f[3].y));
   }
 };
 template <> struct Pack16<__half> {
@@ -110,6 +123,12 @@ template <> struct Pack16<__half> {
   static __device__ __forceinline__ uint4 pack(const float (&f)[8]) {
     return make_uint4(two(f[0], f[1]), two(f[2], f[3]), two(f[4], f[5]), two(f[6], f[7]));
   }
+  static __device__ __forceinline__ void unpack(const uint4& u, float2 (&f)[4]) {
+    word(u.x, f[0].x, f[0].y); word(u.y, f[1].x, f[1].y); word(u.z, f[2].x, f[2].y); word(u.w, f[3].x, f[3].y);
+  }
+  static __device__ __forceinline__ uint4 pack(const float2 (&f)[4]) {
+    return make_uint4(two(f[0].x, f[0].y), two(f[1].x, f[1].y), two(f[2].x, f[2].y), two(f[3].x, f[3].y));
+  }
 };
 
 // ---------------------------------------------------------------------------
@@ -122,6 +141,16 @@ __device__ __forceinline__ float fmul(float a, float b) { return __fmul_rn(a, b)
 __device__ __forceinline__ float fadd(float a, float b) { return __fadd_rn(a, b); }
 __device__ __forceinline__ float fsub(float a, float b) { return __fsub_rn(a, b); }
 __device__ __forceinline__ float ffma(float a, float b, float c) { return __fmaf_rn(a, b, c); }
+
+// Packed pairs: one sm_100-family instruction (add / mul / fma .rn.f32x2)
+// applies the operation to both lanes, each rounded exactly as the scalar
+// form above, so a loop over pairs gives the bits of the loop over elements
+// with half the floating-point instructions.  a - b is written a + (-b),
+// which is the same IEEE operation.
+__device__ __forceinline__ float2 f2s(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
 // ---------------------------------------------------------------------------
 // Reductions.  Butterfly shuffles give every lane the same sum (each step adds
@@ -166,6 +195,12 @@ template <int VEC>
 __device__ __forceinline__ float tree_sum(const float (&a)[VEC]) {
   if constexpr (VEC == 4) return fadd(fadd(a[0], a[1]), fadd(a[2], a[3]));
   else return fadd(fadd(fadd(a[0], a[1]), fadd(a[2], a[3])), fadd(fadd(a[4], a[5]), fadd(a[6], a[7])));
+}
+// The same sum over accumulators held as pairs (lanes 2h, 2h+1 in a[h]).
+template <int H>
+__device__ __forceinline__ float tree_sum(const float2 (&a)[H]) {
+  if constexpr (H == 2) return fadd(fadd(a[0].x, a[0].y), fadd(a[1].x, a[1].y));
+  else return fadd(fadd(fadd(a[0].x, a[0].y), fadd(a[1].x, a[1].y)), fadd(fadd(a[2].x, a[2].y), fadd(a[3].x, a[3].y)));
 }
 
 // 1/sqrt(m + eps).

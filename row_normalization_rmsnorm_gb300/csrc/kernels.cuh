@@ -63,6 +63,7 @@ __host__ __device__ constexpr size_t staged_col_bytes(int N, bool wreg) {
 template <int OP, class T, class TW, int NPT, bool DW, bool DB>
 __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const int S) {
   constexpr int VEC = 16 / (int)sizeof(T);
+  constexpr int H = VEC / 2;   // element pairs per chunk
   constexpr bool LN = (OP == LN_FWD || OP == LN_BWD);
   constexpr bool BWD = OpInfo<OP>::BWD;
   // Up to 4 chunks per thread, W' (and the bias) live in registers; at 8
@@ -99,9 +100,11 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
 
   grid_dependency_wait();
 
-  const int64_t G = gridDim.x;
-  const int64_t row0 = blockIdx.x;
-  const int64_t nrows = (p.M - row0 + G - 1) / G;   // >= 1: the grid never exceeds M
+  // Row counters of this CTA are 32-bit: the launcher guarantees that no CTA
+  // owns 2^31 or more rows.
+  const int G = gridDim.x;
+  const int row0 = blockIdx.x;
+  const int nrows = (int)((p.M - row0 + G - 1) / G);   // >= 1: the grid never exceeds M
   const uint64_t pol = l2_policy_evict_first();
   const char* g0 = static_cast<const char*>(p.in0);
   const char* g1 = static_cast<const char*>(p.in1);
@@ -110,11 +113,11 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
   // Producer state (thread 0): rows of this CTA whose copies have been
   // issued, and the stage the next one goes to.  Stage and phase indices
   // advance by counting, never by dividing the row index.
-  int64_t issued = 0;
+  int issued = 0;
   int istage = 0;
 
   auto issue_next = [&]() {
-    const int64_t row = row0 + issued * G;
+    const int64_t row = row0 + (int64_t)issued * G;
     unsigned char* dst = stages + (size_t)istage * stage_bytes;
     uint64_t* bar = &bars[istage];
     fence_proxy_async_smem();
@@ -136,51 +139,58 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
   }
 
   // Per-thread constant columns: W' = float(w) + offset (and the LayerNorm
-  // bias) in FP32, formed once per CTA.
-  float wv[NWR][VEC];
-  float bv[NB][VEC];
+  // bias) in FP32, formed once per CTA.  Elementwise values are held as
+  // pairs (float2, lanes 2h and 2h+1 of a chunk) for the packed FP32
+  // instructions.
+  float2 wv[NWR][H];
+  float2 bv[NB][H];
   const bool has_b = (OP == LN_FWD) && p.b != nullptr;
   const TW* wp = static_cast<const TW*>(p.w);
 #pragma unroll
   for (int j = 0; j < NPT; ++j) {
     const int c = tid + j * nt;
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) {
-      const float wj = (c < nchunks) ? fadd(to_f(wp[c * VEC + v]), p.offset) : 0.f;
-      const float bj = (has_b && c < nchunks) ? to_f(static_cast<const TW*>(p.b)[c * VEC + v]) : 0.f;
+    for (int h = 0; h < H; ++h) {
+      float wj[2], bj[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int col = c * VEC + 2 * h + e;
+        wj[e] = (c < nchunks) ? fadd(to_f(wp[col]), p.offset) : 0.f;
+        bj[e] = (has_b && c < nchunks) ? to_f(static_cast<const TW*>(p.b)[col]) : 0.f;
+      }
       if constexpr (WREG) {
-        wv[j][v] = wj;
-        if constexpr (OP == LN_FWD) bv[j][v] = bj;
+        wv[j][h] = make_float2(wj[0], wj[1]);
+        if constexpr (OP == LN_FWD) bv[j][h] = make_float2(bj[0], bj[1]);
       } else if (c < nchunks) {
-        wsm[c * VEC + v] = wj;
-        if constexpr (OP == LN_FWD) wsm[N + c * VEC + v] = bj;
+        reinterpret_cast<float2*>(wsm)[c * H + h] = make_float2(wj[0], wj[1]);
+        if constexpr (OP == LN_FWD) reinterpret_cast<float2*>(wsm + N)[c * H + h] = make_float2(bj[0], bj[1]);
       }
     }
   }
-  // W' (or the bias) of chunk c, slot j, into w[VEC]
-  auto colv = [&](int j, int c, int which, float (&w)[VEC]) {
+  // W' (or the bias) of chunk c, slot j, into w[H]
+  auto colv = [&](int j, int c, int which, float2 (&w)[H]) {
     if constexpr (WREG) {
 #pragma unroll
-      for (int v = 0; v < VEC; ++v) w[v] = which ? bv[NB > 1 ? j : 0][v] : wv[j][v];
+      for (int h = 0; h < H; ++h) w[h] = which ? bv[NB > 1 ? j : 0][h] : wv[j][h];
     } else {
       const float4* q = reinterpret_cast<const float4*>(wsm + (which ? N : 0) + c * VEC);
 #pragma unroll
-      for (int v = 0; v < VEC; v += 4) {
-        const float4 t = q[v / 4];
-        w[v] = t.x; w[v + 1] = t.y; w[v + 2] = t.z; w[v + 3] = t.w;
+      for (int h = 0; h < H; h += 2) {
+        const float4 t = q[h / 2];
+        w[h] = make_float2(t.x, t.y); w[h + 1] = make_float2(t.z, t.w);
       }
     }
   };
-  float dwa[NDW][VEC];
-  float dba[NDB][VEC];
+  float2 dwa[NDW][H];
+  float2 dba[NDB][H];
 #pragma unroll
   for (int j = 0; j < NDW; ++j)
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) dwa[j][v] = 0.f;
+    for (int h = 0; h < H; ++h) dwa[j][h] = f2s(0.f);
 #pragma unroll
   for (int j = 0; j < NDB; ++j)
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) dba[j][v] = 0.f;
+    for (int h = 0; h < H; ++h) dba[j][h] = f2s(0.f);
 
   __syncthreads();   // ring initialised (and first copies issued) by thread 0
 
@@ -195,12 +205,12 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
   }
 
   int bank = 0;
-  int64_t k = 0;
+  int k = 0;
   int s = 0;            // stage of row k
   uint32_t phase = 0;   // parity of that stage's current use
   bool aborted = false;
   for (; k < nrows; ++k, (++s == S) ? (s = 0, phase ^= 1u) : 0) {
-    const int64_t row = row0 + k * G;
+    const int64_t row = row0 + (int64_t)k * G;
     const int fl = (int)(k & 1);
     float mean = 0.f, rstd = 0.f;
     if (have_stats) {
@@ -235,47 +245,48 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
       // about the mean found in the previous barrier) together with the sum
       // of row k+1.  Rows k and k+1 are resident (the ring has >= 3 stages).
       if (k == 0) {
-        float acc[VEC];
+        float2 acc[H];
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+        for (int h = 0; h < H; ++h) acc[h] = f2s(0.f);
 #pragma unroll
         for (int j = 0; j < NPT; ++j) {
           const int c = tid + j * nt;
           if (c < nchunks) {
-            float t[VEC];
+            float2 t[H];
             P::unpack(r0[c], t);
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) acc[v] = fadd(acc[v], t[v]);
+            for (int h = 0; h < H; ++h) acc[h] = fadd2(acc[h], t[h]);
           }
         }
-        float a[1] = {tree_sum<VEC>(acc)};
+        float a[1] = {tree_sum<H>(acc)};
         block_sum<1>(a, red, bank);
         after_first_barrier();
         mu_next = div_n(a[0], inv_n);
       }
       mean = mu_next;
-      float xf[NX][VEC];
-      float accv[VEC], accs[VEC];
+      const float2 nmean = f2s(-mean);
+      float2 xf[NX][H];
+      float2 accv[H], accs[H];
 #pragma unroll
-      for (int v = 0; v < VEC; ++v) { accv[v] = 0.f; accs[v] = 0.f; }
+      for (int h = 0; h < H; ++h) { accv[h] = f2s(0.f); accs[h] = f2s(0.f); }
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
         const int c = tid + j * nt;
-        float t[VEC];
+        float2 t[H];
         if (c < nchunks) {
           P::unpack(r0[c], t);
 #pragma unroll
-          for (int v = 0; v < VEC; ++v) {
-            const float d = fsub(t[v], mean);
-            accv[v] = ffma(d, d, accv[v]);
+          for (int h = 0; h < H; ++h) {
+            const float2 d = fadd2(t[h], nmean);
+            accv[h] = ffma2(d, d, accv[h]);
           }
         } else {
 #pragma unroll
-          for (int v = 0; v < VEC; ++v) t[v] = 0.f;
+          for (int h = 0; h < H; ++h) t[h] = f2s(0.f);
         }
         if constexpr (KEEP) {
 #pragma unroll
-          for (int v = 0; v < VEC; ++v) xf[j][v] = t[v];
+          for (int h = 0; h < H; ++h) xf[j][h] = t[h];
         }
       }
       if (k + 1 < nrows) {
@@ -290,14 +301,14 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
         for (int j = 0; j < NPT; ++j) {
           const int c = tid + j * nt;
           if (c < nchunks) {
-            float t[VEC];
+            float2 t[H];
             P::unpack(n0[c], t);
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) accs[v] = fadd(accs[v], t[v]);
+            for (int h = 0; h < H; ++h) accs[h] = fadd2(accs[h], t[h]);
           }
         }
       }
-      float a2[2] = {tree_sum<VEC>(accv), tree_sum<VEC>(accs)};
+      float a2[2] = {tree_sum<H>(accv), tree_sum<H>(accs)};
       block_sum<2>(a2, red, bank);
       after_first_barrier();
       rstd = inv_rms(div_n(a2[0], inv_n), p.eps);
@@ -307,22 +318,23 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
         if (p.rstd_out) p.rstd_out[row] = rstd;
         if (p.mean_out) p.mean_out[row] = mean;
       }
+      const float2 rs2 = f2s(rstd);
       T* yrow = static_cast<T*>(p.out0) + row * p.s_out0;
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
         const int c = tid + j * nt;
         if (c < nchunks) {
-          float t[VEC], w[VEC], bb[VEC], yf[VEC];
+          float2 t[H], w[H], bb[H], yf[H];
           if constexpr (KEEP) {
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) t[v] = xf[j][v];
+            for (int h = 0; h < H; ++h) t[h] = xf[j][h];
           } else {
             P::unpack(r0[c], t);
           }
           colv(j, c, 0, w);
           colv(j, c, 1, bb);
 #pragma unroll
-          for (int v = 0; v < VEC; ++v) yf[v] = ffma(fmul(fsub(t[v], mean), rstd), w[v], bb[v]);
+          for (int h = 0; h < H; ++h) yf[h] = ffma2(fmul2(fadd2(t[h], nmean), rs2), w[h], bb[h]);
           st_global_cs16(yrow + (int64_t)c * VEC, P::pack(yf));
         }
       }
@@ -330,61 +342,61 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
       // ---- forward: the row (x, or h = x + residual) in FP32 -------------
       // row value of chunk c: x, or h = x + residual (FP32, exact for 16-bit
       // inputs); kept in registers (xf) or re-read from the stage
-      auto rowv = [&](int c, float (&o)[VEC]) {
+      auto rowv = [&](int c, float2 (&o)[H]) {
         P::unpack(r0[c], o);
         if constexpr (OP == FADD_FWD) {
-          float rf[VEC];
+          float2 rf[H];
           P::unpack(r1[c], rf);
 #pragma unroll
-          for (int v = 0; v < VEC; ++v) o[v] = fadd(o[v], rf[v]);
+          for (int h = 0; h < H; ++h) o[h] = fadd2(o[h], rf[h]);
         }
       };
-      float xf[NX][VEC];
-      float acc[VEC];
+      float2 xf[NX][H];
+      float2 acc[H];
 #pragma unroll
-      for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+      for (int h = 0; h < H; ++h) acc[h] = f2s(0.f);
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
         const int c = tid + j * nt;
         if (c < nchunks) {
-          float t[VEC];
+          float2 t[H];
           rowv(c, t);
           if constexpr (OP == FADD_FWD) {
             // the residual stream passed on: h rounded once to T
             st_global_cs16(static_cast<T*>(p.out1) + row * p.s_out1 + (int64_t)c * VEC, P::pack(t));
           }
 #pragma unroll
-          for (int v = 0; v < VEC; ++v) {
-            if constexpr (KEEP) xf[j][v] = t[v];
-            if constexpr (LN) acc[v] = fadd(acc[v], t[v]);
-            else              acc[v] = ffma(t[v], t[v], acc[v]);
+          for (int h = 0; h < H; ++h) {
+            if constexpr (KEEP) xf[j][h] = t[h];
+            acc[h] = ffma2(t[h], t[h], acc[h]);
           }
         } else if constexpr (KEEP) {
 #pragma unroll
-          for (int v = 0; v < VEC; ++v) xf[j][v] = 0.f;
+          for (int h = 0; h < H; ++h) xf[j][h] = f2s(0.f);
         }
       }
-      float a[1] = {tree_sum<VEC>(acc)};
+      float a[1] = {tree_sum<H>(acc)};
       block_sum<1>(a, red, bank);
       after_first_barrier();
       rstd = inv_rms(div_n(a[0], inv_n), p.eps);
       if (abort_flag[fl]) { aborted = true; break; }
       if (tid == 0 && p.rstd_out) p.rstd_out[row] = rstd;
+      const float2 rs2 = f2s(rstd);
       T* yrow = static_cast<T*>(p.out0) + row * p.s_out0;
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
         const int c = tid + j * nt;
         if (c < nchunks) {
-          float t[VEC], w[VEC], yf[VEC];
+          float2 t[H], w[H], yf[H];
           if constexpr (KEEP) {
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) t[v] = xf[j][v];
+            for (int h = 0; h < H; ++h) t[h] = xf[j][h];
           } else {
             rowv(c, t);
           }
           colv(j, c, 0, w);
 #pragma unroll
-          for (int v = 0; v < VEC; ++v) yf[v] = fmul(fmul(t[v], rstd), w[v]);
+          for (int h = 0; h < H; ++h) yf[h] = fmul2(fmul2(t[h], rs2), w[h]);
           st_global_cs16(yrow + (int64_t)c * VEC, P::pack(yf));
         }
       }
@@ -393,108 +405,113 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
       if (!have_stats) {
         // statistics recomputed from the saved row (same arithmetic as the
         // forward: two passes for LayerNorm)
-        float acc[VEC];
+        float2 acc[H];
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+        for (int h = 0; h < H; ++h) acc[h] = f2s(0.f);
 #pragma unroll
         for (int j = 0; j < NPT; ++j) {
           const int c = tid + j * nt;
           if (c < nchunks) {
-            float xf[VEC];
+            float2 xf[H];
             P::unpack(r0[c], xf);
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) {
-              if constexpr (LN) acc[v] = fadd(acc[v], xf[v]);
-              else              acc[v] = ffma(xf[v], xf[v], acc[v]);
+            for (int h = 0; h < H; ++h) {
+              if constexpr (LN) acc[h] = fadd2(acc[h], xf[h]);
+              else              acc[h] = ffma2(xf[h], xf[h], acc[h]);
             }
           }
         }
-        float a[1] = {tree_sum<VEC>(acc)};
+        float a[1] = {tree_sum<H>(acc)};
         block_sum<1>(a, red, bank);
         after_first_barrier();
         if constexpr (LN) {
           mean = div_n(a[0], inv_n);
+          const float2 nmean = f2s(-mean);
 #pragma unroll
-          for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+          for (int h = 0; h < H; ++h) acc[h] = f2s(0.f);
 #pragma unroll
           for (int j = 0; j < NPT; ++j) {
             const int c = tid + j * nt;
             if (c < nchunks) {
-              float xf[VEC];
+              float2 xf[H];
               P::unpack(r0[c], xf);
 #pragma unroll
-              for (int v = 0; v < VEC; ++v) {
-                const float d = fsub(xf[v], mean);
-                acc[v] = ffma(d, d, acc[v]);
+              for (int h = 0; h < H; ++h) {
+                const float2 d = fadd2(xf[h], nmean);
+                acc[h] = ffma2(d, d, acc[h]);
               }
             }
           }
-          float q[1] = {tree_sum<VEC>(acc)};
+          float q[1] = {tree_sum<H>(acc)};
           block_sum<1>(q, red, bank);
           rstd = inv_rms(div_n(q[0], inv_n), p.eps);
         } else {
           rstd = inv_rms(div_n(a[0], inv_n), p.eps);
         }
       }
+      const float2 rs2 = f2s(rstd);
+      const float2 nmean = f2s(-mean);
       // row sums of g (LayerNorm) and g * xhat
-      float acc0[VEC], acc1[VEC];
+      float2 acc0[H], acc1[H];
 #pragma unroll
-      for (int v = 0; v < VEC; ++v) { acc0[v] = 0.f; acc1[v] = 0.f; }
+      for (int h = 0; h < H; ++h) { acc0[h] = f2s(0.f); acc1[h] = f2s(0.f); }
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
         const int c = tid + j * nt;
         if (c < nchunks) {
-          float xf[VEC], df[VEC], w[VEC];
+          float2 xf[H], df[H], w[H];
           P::unpack(r0[c], xf);
           P::unpack(r1[c], df);
           colv(j, c, 0, w);
 #pragma unroll
-          for (int v = 0; v < VEC; ++v) {
-            const float g = fmul(df[v], w[v]);
+          for (int h = 0; h < H; ++h) {
+            const float2 g = fmul2(df[h], w[h]);
             if constexpr (LN) {
-              const float xh = fmul(fsub(xf[v], mean), rstd);
-              acc0[v] = fadd(acc0[v], g);
-              acc1[v] = ffma(g, xh, acc1[v]);
+              const float2 xh = fmul2(fadd2(xf[h], nmean), rs2);
+              acc0[h] = fadd2(acc0[h], g);
+              acc1[h] = ffma2(g, xh, acc1[h]);
             } else {
-              acc1[v] = ffma(g, fmul(xf[v], rstd), acc1[v]);
+              acc1[h] = ffma2(g, fmul2(xf[h], rs2), acc1[h]);
             }
           }
         }
       }
       float a[NR];
-      if constexpr (LN) { a[0] = tree_sum<VEC>(acc0); a[NR - 1] = tree_sum<VEC>(acc1); }
-      else              { a[0] = tree_sum<VEC>(acc1); }
+      if constexpr (LN) { a[0] = tree_sum<H>(acc0); a[NR - 1] = tree_sum<H>(acc1); }
+      else              { a[0] = tree_sum<H>(acc1); }
       block_sum<NR>(a, red, bank);
       after_first_barrier();
       if (abort_flag[fl]) { aborted = true; break; }
-      const float mg = LN ? div_n(a[0], inv_n) : 0.f;
-      const float mgx = div_n(a[NR - 1], inv_n);
+      // dx = rstd * (g - xhat * mean(g xhat) - mean(g)), the products and
+      // differences written as fused multiply-adds of negated row constants
+      const float2 nmg = f2s(LN ? -div_n(a[0], inv_n) : 0.f);
+      const float2 nmgx = f2s(-div_n(a[NR - 1], inv_n));
       const bool has_dh = (OP == FADD_BWD) && nin > 2;
       T* dxrow = static_cast<T*>(p.out0) + row * p.s_out0;
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
         const int c = tid + j * nt;
         if (c < nchunks) {
-          float xf[VEC], df[VEC], hf[VEC], of[VEC], w[VEC];
+          float2 xf[H], df[H], hf[H], of[H], w[H];
           P::unpack(r0[c], xf);
           P::unpack(r1[c], df);
           if (has_dh) P::unpack(r2[c], hf);
           colv(j, c, 0, w);
 #pragma unroll
-          for (int v = 0; v < VEC; ++v) {
-            const float g = fmul(df[v], w[v]);
-            float xh, dx;
+          for (int h = 0; h < H; ++h) {
+            const float2 g = fmul2(df[h], w[h]);
+            float2 xh, dx;
             if constexpr (LN) {
-              xh = fmul(fsub(xf[v], mean), rstd);
-              dx = fmul(rstd, ffma(-xh, mgx, fsub(g, mg)));
+              xh = fmul2(fadd2(xf[h], nmean), rs2);
+              dx = fmul2(rs2, ffma2(xh, nmgx, fadd2(g, nmg)));
             } else {
-              xh = fmul(xf[v], rstd);
-              dx = fmul(rstd, ffma(-xh, mgx, g));
+              xh = fmul2(xf[h], rs2);
+              dx = fmul2(rs2, ffma2(xh, nmgx, g));
             }
-            if (has_dh) dx = fadd(dx, hf[v]);
-            of[v] = dx;
-            if constexpr (DW) dwa[j][v] = ffma(df[v], xh, dwa[j][v]);
-            if constexpr (DB) dba[j][v] = fadd(dba[j][v], df[v]);
+            if (has_dh) dx = fadd2(dx, hf[h]);
+            of[h] = dx;
+            if constexpr (DW) dwa[j][h] = ffma2(df[h], xh, dwa[j][h]);
+            if constexpr (DB) dba[j][h] = fadd2(dba[j][h], df[h]);
           }
           st_global_cs16(dxrow + (int64_t)c * VEC, P::pack(of));
         }
@@ -507,7 +524,7 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
     // Bounded drain of the copies still in flight into this CTA's shared
     // memory (rows k .. issued-1), then leave without writing partial sums.
     if (tid == 0) {
-      for (int64_t kk = k; kk < issued; ++kk) {
+      for (int kk = k; kk < issued; ++kk) {
         (void)mbar_wait_bounded(&bars[s], phase);
         if (++s == S) { s = 0; phase ^= 1u; }
       }
@@ -522,11 +539,13 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
       if (c < nchunks) {
         const int64_t off = (int64_t)blockIdx.x * N + (int64_t)c * VEC;
 #pragma unroll
-        for (int v = 0; v < VEC; v += 4) {
+        for (int h = 0; h < H; h += 2) {
           if constexpr (DW)
-            *reinterpret_cast<float4*>(p.ws_dw + off + v) = make_float4(dwa[j][v], dwa[j][v + 1], dwa[j][v + 2], dwa[j][v + 3]);
+            *reinterpret_cast<float4*>(p.ws_dw + off + 2 * h) =
+                make_float4(dwa[j][h].x, dwa[j][h].y, dwa[j][h + 1].x, dwa[j][h + 1].y);
           if constexpr (DB)
-            *reinterpret_cast<float4*>(p.ws_db + off + v) = make_float4(dba[j][v], dba[j][v + 1], dba[j][v + 2], dba[j][v + 3]);
+            *reinterpret_cast<float4*>(p.ws_db + off + 2 * h) =
+                make_float4(dba[j][h].x, dba[j][h].y, dba[j][h + 1].x, dba[j][h + 1].y);
         }
       }
     }
@@ -764,6 +783,8 @@ int launch_staged(const RowParams& p, const DevInfo& di, int nin, int max_ctas, 
   int64_t G = (int64_t)di.sms * ctas;
   if (G > p.M) G = p.M;
   if ((DW || DB) && G > di.max_partial_rows) G = di.max_partial_rows;
+  // the kernel counts a CTA's rows in 32 bits
+  if ((p.M + G - 1) / G > (int64_t)INT32_MAX) return NORM_ERR_UNSUPPORTED_INTERNAL;
   if (launch_pdl(fn, dim3((unsigned)G), dim3(threads), smem, st, p, S) != NORM_OK) return NORM_ERR_CUDA;
   *grid_out = (int)G;
   return NORM_OK;
