@@ -259,8 +259,10 @@ GB300NORM_API int norm_debug_set_path(int mode);
 
 /*
  * Test hook for launch-shape sweeps: key 1 = 16-byte chunks per thread of the
- * aligned-row kernels (1, 2 or 4), key 2 = maximum CTAs per SM, key 3 =
- * maximum pipeline stages; value 0 restores the automatic choice.  Affects
+ * aligned-row kernels (1, 2, 4 or 8), key 2 = maximum CTAs per SM, key 3 =
+ * maximum pipeline stages, key 4 = cap on row bytes in flight per SM in
+ * units of 16 KB (64 = no cap in practice); value 0 restores the automatic
+ * choice (values 0..64).  Affects
  * speed only, never results of the same kernel family except through the
  * reduction tree shape.  Returns NORM_OK or NORM_ERR_ARG.
  */

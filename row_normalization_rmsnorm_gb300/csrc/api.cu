@@ -25,7 +25,7 @@ int cuda_fail(cudaError_t e) {
 namespace {
 
 std::atomic<int> g_force_path{0};
-std::atomic<int> g_tune[4] = {{0}, {0}, {0}, {0}};
+std::atomic<int> g_tune[5] = {{0}, {0}, {0}, {0}, {0}};
 
 int elem_size(int dt) {
   switch (dt) {
@@ -77,6 +77,7 @@ int get_device(DevInfo* out, int** status) {
   out->tune_npt = g_tune[1].load();
   out->tune_max_ctas = g_tune[2].load();
   out->tune_max_stages = g_tune[3].load();
+  out->tune_inflight_16k = g_tune[4].load();
   if (status) *status = g_dev.status[dev];
   return NORM_OK;
 }
@@ -164,7 +165,7 @@ int check_vec_f32(const void* p) {
 }
 
 int64_t ws_bytes_needed(int64_t M, int64_t N, int sms, int nbuf) {
-  return partial_rows(M, sms) * N * 4 * nbuf;
+  return partial_rows(M, N, sms) * N * 4 * nbuf;
 }
 
 // The workspace pointer is checked before the device is queried for its size.
@@ -200,7 +201,7 @@ template <class F>
 int run_bwd(RowParams& p, int64_t M, int64_t N, void* dw, void* db, int dw_dtype, void* ws, size_t ws_bytes,
             const DevInfo& di, cudaStream_t st, F&& launch_rows) {
   if (M == 0) return launch_colreduce(nullptr, dw, nullptr, db, 0, (int)N, dw_dtype, st);
-  const int64_t rows = partial_rows(M, di.sms);
+  const int64_t rows = partial_rows(M, N, di.sms);
   float* wsf = static_cast<float*>(ws);
   p.ws_dw = dw ? wsf : nullptr;
   p.ws_db = db ? wsf + (dw ? rows * N : 0) : nullptr;
@@ -245,7 +246,7 @@ int norm_debug_set_path(int mode) {
 }
 
 int norm_debug_tune(int key, int value) {
-  if (key < 1 || key > 3 || value < 0 || value > 64) return NORM_ERR_ARG;
+  if (key < 1 || key > 4 || value < 0 || value > 64) return NORM_ERR_ARG;
   g_tune[key].store(value);
   return NORM_OK;
 }
@@ -394,7 +395,7 @@ int norm_rms_bwd(const void* dy, int64_t dy_stride, const void* x, int64_t x_str
                      vec_span(need ? workspace : nullptr, need, 1, true)};
   RETURN_IF(check_overlaps(sp, 7));
   if (!status) RETURN_IF(get_device(&di, &status));
-  di.max_partial_rows = partial_rows(M, di.sms);
+  di.max_partial_rows = partial_rows(M, N, di.sms);
   RowParams p = base_params(M, N, offset, eps, w, status);
   p.in0 = x; p.s_in0 = x_stride;
   p.in1 = dy; p.s_in1 = dy_stride;
@@ -441,7 +442,7 @@ int norm_ln_bwd(const void* dy, int64_t dy_stride, const void* x, int64_t x_stri
                      vec_span(need ? workspace : nullptr, need, 1, true)};
   RETURN_IF(check_overlaps(sp, 9));
   if (!status) RETURN_IF(get_device(&di, &status));
-  di.max_partial_rows = partial_rows(M, di.sms);
+  di.max_partial_rows = partial_rows(M, N, di.sms);
   RowParams p = base_params(M, N, offset, eps, w, status);
   p.in0 = x; p.s_in0 = x_stride;
   p.in1 = dy; p.s_in1 = dy_stride;
@@ -485,7 +486,7 @@ int norm_fused_add_rms_bwd(const void* dy, int64_t dy_stride, const void* dh_out
                      vec_span(dw, N, dws, true), vec_span(need ? workspace : nullptr, need, 1, true)};
   RETURN_IF(check_overlaps(sp, 8));
   if (!status) RETURN_IF(get_device(&di, &status));
-  di.max_partial_rows = partial_rows(M, di.sms);
+  di.max_partial_rows = partial_rows(M, N, di.sms);
   RowParams p = base_params(M, N, offset, eps, w, status);
   p.in0 = h; p.s_in0 = h_stride;
   p.in1 = dy; p.s_in1 = dy_stride;

@@ -145,8 +145,12 @@ __device__ __forceinline__ float ffma(float a, float b, float c) { return __fmaf
 // Packed pairs: one sm_100-family instruction (add / mul / fma .rn.f32x2)
 // applies the operation to both lanes, each rounded exactly as the scalar
 // form above, so a loop over pairs gives the bits of the loop over elements
-// with half the floating-point instructions.  a - b is written a + (-b),
-// which is the same IEEE operation.
+// with half the floating-point instructions.  Unlike the scalar forms, a
+// packed multiply whose result feeds a packed add may still be fused into
+// one FMA by the compiler, and whether it is differs between
+// instantiations.  The kernels therefore never write that pattern: where a
+// product meets a sum they call ffma2 themselves.  a - b is written
+// a + (-b), the same IEEE operation.
 __device__ __forceinline__ float2 f2s(float a) { return make_float2(a, a); }
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }

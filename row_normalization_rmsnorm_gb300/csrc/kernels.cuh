@@ -49,6 +49,7 @@ __device__ __forceinline__ float div_n(float s, float inv_n) { return fmul(s, in
 // ===========================================================================
 constexpr int kStagedHeader = 1024;   // bytes: S mbarriers (<= 32) + reduction banks
 constexpr int kMaxStages = 16;
+constexpr int kInflightUnits = 8;     // default cap on row bytes in flight per SM, x 16 KB
 // Where a staged instantiation keeps W' (and the bias): registers up to 4
 // chunks per thread, shared memory beyond.
 __host__ __device__ constexpr bool staged_wreg(int npt) { return npt <= 4; }
@@ -468,7 +469,7 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
             const float2 g = fmul2(df[h], w[h]);
             if constexpr (LN) {
               const float2 xh = fmul2(fadd2(xf[h], nmean), rs2);
-              acc0[h] = fadd2(acc0[h], g);
+              acc0[h] = ffma2(df[h], w[h], acc0[h]);   // sum of g, each product unrounded
               acc1[h] = ffma2(g, xh, acc1[h]);
             } else {
               acc1[h] = ffma2(g, fmul2(xf[h], rs2), acc1[h]);
@@ -482,8 +483,11 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
       block_sum<NR>(a, red, bank);
       after_first_barrier();
       if (abort_flag[fl]) { aborted = true; break; }
-      // dx = rstd * (g - xhat * mean(g xhat) - mean(g)), the products and
-      // differences written as fused multiply-adds of negated row constants
+      // dx = rstd * (g - xhat * mean(g xhat) - mean(g)) + dh, written as fused
+      // multiply-adds of negated row constants; where a product meets a sum
+      // the two are one fused multiply-add (dy * W' - mean(g), and the
+      // residual gradient added to rstd * (...)), never a rounded product
+      // followed by an add, which the compiler could fuse on its own.
       const float2 nmg = f2s(LN ? -div_n(a[0], inv_n) : 0.f);
       const float2 nmgx = f2s(-div_n(a[NR - 1], inv_n));
       const bool has_dh = (OP == FADD_BWD) && nin > 2;
@@ -499,16 +503,15 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
           colv(j, c, 0, w);
 #pragma unroll
           for (int h = 0; h < H; ++h) {
-            const float2 g = fmul2(df[h], w[h]);
-            float2 xh, dx;
+            float2 xh, t;
             if constexpr (LN) {
               xh = fmul2(fadd2(xf[h], nmean), rs2);
-              dx = fmul2(rs2, ffma2(xh, nmgx, fadd2(g, nmg)));
+              t = ffma2(xh, nmgx, ffma2(df[h], w[h], nmg));
             } else {
               xh = fmul2(xf[h], rs2);
-              dx = fmul2(rs2, ffma2(xh, nmgx, g));
+              t = ffma2(xh, nmgx, fmul2(df[h], w[h]));
             }
-            if (has_dh) dx = fadd2(dx, hf[h]);
+            const float2 dx = has_dh ? ffma2(rs2, t, hf[h]) : fmul2(rs2, t);
             of[h] = dx;
             if constexpr (DW) dwa[j][h] = ffma2(df[h], xh, dwa[j][h]);
             if constexpr (DB) dba[j][h] = fadd2(dba[j][h], df[h]);
@@ -759,6 +762,11 @@ int launch_staged(const RowParams& p, const DevInfo& di, int nin, int max_ctas, 
   if (nb < 0) return NORM_ERR_CUDA;
   if (nb == 0) return NORM_ERR_UNSUPPORTED_INTERNAL;
   int ctas = nb < max_ctas ? nb : max_ctas;
+  if (DW || DB) {
+    // no more CTAs per SM than the workspace has partial rows for
+    const int64_t per_sm = (di.max_partial_rows + di.sms - 1) / di.sms;
+    if (per_sm >= 1 && ctas > per_sm) ctas = (int)per_sm;
+  }
   int S = 0;
   size_t smem = 0;
   for (; ctas >= 1; --ctas) {
@@ -768,6 +776,13 @@ int launch_staged(const RowParams& p, const DevInfo& di, int nin, int max_ctas, 
     if (per_cta < min_smem) continue;
     S = (int)((per_cta - fixed) / stage_bytes);
     if (S > kMaxStages) S = kMaxStages;
+    // Rows in flight: the S-1 stages ahead of the one being reduced, in
+    // every resident CTA.  Past about 128 KB per SM more of them only slows
+    // the stream down (measured on 8192-wide bf16 rows), so the ring stops
+    // there even where shared memory would hold more.
+    const size_t inflight = (size_t)(di.tune_inflight_16k > 0 ? di.tune_inflight_16k : kInflightUnits) * 16384;
+    const int s_cap = 1 + (int)(inflight / ((size_t)ctas * stage_bytes));
+    if (S > s_cap) S = s_cap > min_stages ? s_cap : min_stages;
     if (di.tune_max_stages >= 2 && S > di.tune_max_stages)
       S = di.tune_max_stages > min_stages ? di.tune_max_stages : min_stages;
     // confirm `ctas` CTAs of this size are resident together
@@ -840,15 +855,20 @@ StagedFit probe_staged(const RowParams& p, const DevInfo& di, int nin) {
 
 // Row kernel for one (op, types, flags): the staged path when every streamed
 // row starts on a 16-byte boundary and fits, else the loop path.  Among the
-// staged shapes (1, 2 or 4 chunks per thread) the choice prefers, in order:
-// no register spills (a few bytes aside), at least two resident CTAs per SM
-// (so one CTA's barrier overlaps another's work), and blocks of about 256
-// threads.
+// staged shapes (1, 2, 4 or 8 chunks per thread) the choice prefers, in
+// order: no register spills (a few bytes aside), at least two resident CTAs
+// per SM (so one CTA's barrier overlaps another's work), at least 3/4 of the
+// threads holding a chunk, and then 4, 2, 8, 1 chunks per thread: four
+// independent chunks give each thread the most memory-level parallelism
+// while W' still fits in registers (measured fastest at N = 4096 and 8192
+// wherever it does not spill).
 template <int OP, class T, class TW, bool DW, bool DB>
 int launch_rows(const RowParams& p, const DevInfo& di, bool rows_aligned, cudaStream_t st, int* grid_out) {
   constexpr int VEC = 16 / (int)sizeof(T);
   const int nin = (OP == FADD_BWD && p.in2 == nullptr) ? 2 : OpInfo<OP>::NIN;
-  int max_ctas = (DW || DB) ? 2 : 4;
+  // A trainable backward is further held to the partial rows its workspace
+  // has (launch_staged); occupancy bounds both.
+  int max_ctas = 8;
   if (di.tune_max_ctas > 0) max_ctas = di.tune_max_ctas;
   if (rows_aligned && p.N % VEC == 0 && di.force_path != 2) {
     // A backward picks its shape from the instantiation with every weight
@@ -861,13 +881,16 @@ int launch_rows(const RowParams& p, const DevInfo& di, bool rows_aligned, cudaSt
                                probe_staged<OP, T, TW, 4, PDW, PDB>(p, di, nin),
                                probe_staged<OP, T, TW, 8, PDW, PDB>(p, di, nin)};
     const int npts[4] = {1, 2, 4, 8};
+    const int rank[4] = {1, 3, 4, 2};   // preference among chunks per thread
+    const int nchunks = p.N / VEC;
     int best = -1;
     long best_score = -1;
     for (int i = 0; i < 4; ++i) {
       if (!fits[i].ok) continue;
       if (di.tune_npt && npts[i] != di.tune_npt) continue;
-      const int d = fits[i].threads > 256 ? fits[i].threads - 256 : 256 - fits[i].threads;
-      const long score = (fits[i].spills ? 0 : 1000000L) + (fits[i].ctas >= 2 ? 100000L : 0) + (1024 - d);
+      const bool busy = 4L * nchunks >= 3L * fits[i].threads * npts[i];
+      const long score = (fits[i].spills ? 0 : 1000000L) + (fits[i].ctas >= 2 ? 100000L : 0) +
+                         (busy ? 10000L : 0) + rank[i];
       if (score > best_score) { best_score = score; best = i; }
     }
     int rc = NORM_ERR_UNSUPPORTED_INTERNAL;

@@ -51,16 +51,26 @@ struct DevInfo {
   int smem_reserved = 0;     // shared memory the system reserves per CTA
   int64_t max_partial_rows = 0;  // dW/dB partial rows the workspace holds
   int force_path = 0;        // 0 = automatic, 2 = always the loop kernels
-  // test hooks (0 = automatic): staged chunks per thread, CTAs per SM, stages
+  // test hooks (0 = automatic): staged chunks per thread, CTAs per SM,
+  // stages, and the cap on row bytes in flight per SM (units of 16 KB)
   int tune_npt = 0;
   int tune_max_ctas = 0;
   int tune_max_stages = 0;
+  int tune_inflight_16k = 0;
 };
 
-// Partial rows of the dW / dB workspace for M rows on a device with `sms`
-// SMs: at most two row-kernel CTAs per SM write one each.
-inline int64_t partial_rows(int64_t M, int sms) {
-  const int64_t cap = 2 * (int64_t)sms;
+// Partial rows of the dW / dB workspace for M rows of N columns on a device
+// with `sms` SMs: one per row-kernel CTA, and up to k CTAs per SM with
+// k = 16384 / N kept within [2, 8].  Narrow rows get more resident CTAs (the
+// row kernels of a trainable backward need them to keep enough warps in
+// flight) while the partial rows stay near 64 KB x SMs in total, so the
+// column reduction reads about the same bytes whatever N.
+inline int64_t partial_rows_per_sm(int64_t N) {
+  const int64_t k = N > 0 ? 16384 / N : 8;
+  return k < 2 ? 2 : (k > 8 ? 8 : k);
+}
+inline int64_t partial_rows(int64_t M, int64_t N, int sms) {
+  const int64_t cap = partial_rows_per_sm(N) * (int64_t)sms;
   return M < cap ? M : cap;
 }
 

@@ -127,6 +127,18 @@ def test_workspace_query_host_paths(g):
     assert g.lib.norm_bwd_workspace_bytes(0, 64, 1, 1, ctypes.byref(out)) == 0 and out.value == 0
 
 
+def test_debug_tune_keys_and_range(g):
+    # keys 1..4 accept 0..64 (0 = automatic) and leave the library in its
+    # automatic state again; anything else is NORM_ERR_ARG (10)
+    for key in (1, 2, 3, 4):
+        assert g.lib.norm_debug_tune(key, 64) == 0
+        assert g.lib.norm_debug_tune(key, 0) == 0
+    assert g.lib.norm_debug_tune(0, 1) == 10
+    assert g.lib.norm_debug_tune(5, 1) == 10
+    assert g.lib.norm_debug_tune(4, -1) == 10
+    assert g.lib.norm_debug_tune(4, 65) == 10
+
+
 def test_binding_rejects_cpu_tensors(g):
     import torch
     x = torch.zeros(2, 8, dtype=torch.bfloat16)
