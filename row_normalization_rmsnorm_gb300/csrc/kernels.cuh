@@ -205,6 +205,17 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
     if constexpr (LN) mu_next = p.mean_in[row0];
   }
 
+  // LayerNorm forward: this thread's element count n_t (and 1 / n_t) and its
+  // statistics of the row after the current one: shift, mean offset, M2.
+  float ln_nt = 0.f, ln_inv_nt = 0.f, ln_c = 0.f, ln_off = 0.f, ln_m2 = 0.f;
+  if constexpr (OP == LN_FWD) {
+    int nv = 0;
+#pragma unroll
+    for (int j = 0; j < NPT; ++j) nv += (tid + j * nt < nchunks) ? 1 : 0;
+    ln_nt = (float)(nv * VEC);
+    ln_inv_nt = nv ? 1.0f / ln_nt : 0.f;
+  }
+
   int bank = 0;
   int k = 0;
   int s = 0;            // stage of row k
@@ -242,54 +253,59 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
 
     if constexpr (OP == LN_FWD) {
       // ---- LayerNorm forward, statistics software-pipelined -------------
-      // One barrier per row: it reduces the variance of row k (two-pass,
-      // about the mean found in the previous barrier) together with the sum
-      // of row k+1.  Rows k and k+1 are resident (the ring has >= 3 stages).
-      if (k == 0) {
-        float2 acc[H];
+      // Each thread takes, in one pass over its own elements of a row, the
+      // sums S = sum(x - c) and Q = sum((x - c)^2) about a shift c that is
+      // one of those elements, so its M2 = Q - S^2/n loses at most a factor
+      // 1 + n to cancellation.  The CTA merges the threads exactly with the
+      // pairwise update of Chan, Golub and LeVeque: M2 = sum(M2_t) +
+      // sum(n_t d_t^2), d_t = (c_t - mean) + S_t / n_t, the deviation formed
+      // from the small terms so that a large mean costs it nothing.  One
+      // barrier per row reduces the M2 terms of row k (whose mean came from
+      // the previous barrier) together with the sum of row k+1; each row is
+      // read from its stage twice (statistics, output).  Rows k and k+1 are
+      // resident (the ring has >= 3 stages).
+      auto shifted = [&](const uint4* q0, float& c, float& su, float& sq) {
+        float2 as[H], aq[H];
 #pragma unroll
-        for (int h = 0; h < H; ++h) acc[h] = f2s(0.f);
+        for (int h = 0; h < H; ++h) { as[h] = f2s(0.f); aq[h] = f2s(0.f); }
+        c = 0.f;
 #pragma unroll
         for (int j = 0; j < NPT; ++j) {
-          const int c = tid + j * nt;
-          if (c < nchunks) {
+          const int ci = tid + j * nt;
+          if (ci < nchunks) {
             float2 t[H];
-            P::unpack(r0[c], t);
+            P::unpack(q0[ci], t);
+            if (j == 0) c = t[0].x;   // the thread's first element
+            const float2 nc = f2s(-c);
 #pragma unroll
-            for (int h = 0; h < H; ++h) acc[h] = fadd2(acc[h], t[h]);
+            for (int h = 0; h < H; ++h) {
+              const float2 d = fadd2(t[h], nc);
+              as[h] = fadd2(as[h], d);
+              aq[h] = ffma2(d, d, aq[h]);
+            }
           }
         }
-        float a[1] = {tree_sum<H>(acc)};
+        su = tree_sum<H>(as);
+        sq = tree_sum<H>(aq);
+      };
+      // this thread's (shift, mean offset S/n, M2) of a row from its sums
+      auto local = [&](float c, float su, float sq) {
+        const float so = fmul(su, ln_inv_nt);
+        ln_c = c;
+        ln_off = so;
+        ln_m2 = fmaxf(ffma(-su, so, sq), 0.f);
+      };
+      if (k == 0) {
+        float c0, su0, sq0;
+        shifted(r0, c0, su0, sq0);
+        float a[1] = {ffma(ln_nt, c0, su0)};
         block_sum<1>(a, red, bank);
         after_first_barrier();
         mu_next = div_n(a[0], inv_n);
+        local(c0, su0, sq0);
       }
       mean = mu_next;
-      const float2 nmean = f2s(-mean);
-      float2 xf[NX][H];
-      float2 accv[H], accs[H];
-#pragma unroll
-      for (int h = 0; h < H; ++h) { accv[h] = f2s(0.f); accs[h] = f2s(0.f); }
-#pragma unroll
-      for (int j = 0; j < NPT; ++j) {
-        const int c = tid + j * nt;
-        float2 t[H];
-        if (c < nchunks) {
-          P::unpack(r0[c], t);
-#pragma unroll
-          for (int h = 0; h < H; ++h) {
-            const float2 d = fadd2(t[h], nmean);
-            accv[h] = ffma2(d, d, accv[h]);
-          }
-        } else {
-#pragma unroll
-          for (int h = 0; h < H; ++h) t[h] = f2s(0.f);
-        }
-        if constexpr (KEEP) {
-#pragma unroll
-          for (int h = 0; h < H; ++h) xf[j][h] = t[h];
-        }
-      }
+      float c1 = 0.f, su1 = 0.f, sq1 = 0.f;
       if (k + 1 < nrows) {
         const int s1 = (s + 1 == S) ? 0 : s + 1;
         const uint32_t ph1 = (s + 1 == S) ? (phase ^ 1u) : phase;
@@ -297,23 +313,16 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
           atomicOr(p.status, STATUS_WAIT_TIMEOUT);
           abort_flag[fl] = 1;
         }
-        const uint4* n0 = reinterpret_cast<const uint4*>(stages + (size_t)s1 * stage_bytes);
-#pragma unroll
-        for (int j = 0; j < NPT; ++j) {
-          const int c = tid + j * nt;
-          if (c < nchunks) {
-            float2 t[H];
-            P::unpack(n0[c], t);
-#pragma unroll
-            for (int h = 0; h < H; ++h) accs[h] = fadd2(accs[h], t[h]);
-          }
-        }
+        shifted(reinterpret_cast<const uint4*>(stages + (size_t)s1 * stage_bytes), c1, su1, sq1);
       }
-      float a2[2] = {tree_sum<H>(accv), tree_sum<H>(accs)};
+      const float dt = fadd(fsub(ln_c, mean), ln_off);
+      float a2[2] = {ffma(fmul(ln_nt, dt), dt, ln_m2), ffma(ln_nt, c1, su1)};
       block_sum<2>(a2, red, bank);
       after_first_barrier();
       rstd = inv_rms(div_n(a2[0], inv_n), p.eps);
       mu_next = div_n(a2[1], inv_n);
+      local(c1, su1, sq1);
+      const float2 nmean = f2s(-mean);
       if (abort_flag[fl]) { aborted = true; break; }
       if (tid == 0) {
         if (p.rstd_out) p.rstd_out[row] = rstd;
@@ -326,12 +335,7 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
         const int c = tid + j * nt;
         if (c < nchunks) {
           float2 t[H], w[H], bb[H], yf[H];
-          if constexpr (KEEP) {
-#pragma unroll
-            for (int h = 0; h < H; ++h) t[h] = xf[j][h];
-          } else {
-            P::unpack(r0[c], t);
-          }
+          P::unpack(r0[c], t);
           colv(j, c, 0, w);
           colv(j, c, 1, bb);
 #pragma unroll
