@@ -317,9 +317,14 @@ def main():
     ap.add_argument("--no-shapes", action="store_true", help="skip the per-shape table")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the frozen timings, the e2e run and the CPU baseline (profiling)")
+    ap.add_argument("--grid", action="store_true",
+                    help="run every operation of the shape grid twice, untimed, and print the call order "
+                         "(for an ncu kernel-duration capture)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.grid:
+        return run_grid()
 
     import row_normalization_rmsnorm_gb300 as g
     from row_normalization_rmsnorm_gb300 import dist as gdist
@@ -446,6 +451,44 @@ def main():
 GRID_SHAPES = [(2048, 4096), (4096, 4096), (4096, 8192), (8192, 4096), (8192, 8192)]
 GEMMA_SHAPES = [(1, 4096), (128, 4096), (2048, 4096), (8192, 4096), (128, 8192), (2048, 8192), (128, 18432)]
 FADD_SHAPES = [(128, 4096), (2048, 4096), (2048, 8192)]
+
+
+def grid_families():
+    """(M, N) -> operation families of the shape grid: RMSNorm and LayerNorm on
+    the bf16 grid, FusedAdd on its shapes and at 8192x8192, RMSNorm on the
+    Gemma shapes."""
+    fams = {}
+    for sh in GRID_SHAPES:
+        fams.setdefault(sh, []).extend(["rms", "ln"])
+    for sh in FADD_SHAPES + [(8192, 8192)]:
+        fams.setdefault(sh, []).append("fadd")
+    for sh in GEMMA_SHAPES:
+        if "rms" not in fams.setdefault(sh, []):
+            fams[sh].append("rms")
+    return fams
+
+
+def run_grid():
+    """Each (shape, operation) of grid_families() twice -- forward, trainable
+    backward, frozen backward -- with nothing timed, so that an ncu launch
+    list (gpu__time_duration) gives every kernel's duration; the JSON line
+    lists the calls in launch order (a trainable backward launches its row
+    kernel and then the column reduce)."""
+    import row_normalization_rmsnorm_gb300 as g
+    st = torch.cuda.current_stream()
+    order = []
+    for (M, N), fams in grid_families().items():
+        wl = Workload(g, host_inputs(M, N, 0), M, N)
+        for fam in fams:
+            for op, tr in [(fam + "_fwd", True), (fam + "_bwd", True), (fam + "_bwd", False)]:
+                for rep in range(2):
+                    wl.run(op, tr, st)
+                    order.append([M, N, op, tr, rep])
+        torch.cuda.synchronize()
+        del wl
+        torch.cuda.empty_cache()
+    print(json.dumps({"grid_order": order}), flush=True)
+    return 0
 
 
 def shape_table(g, flush_l2, reps=40):

@@ -4,9 +4,12 @@
 // this kernel owns 32 adjacent columns: its 8 warps sum interleaved subsets of
 // the partial rows (warp k takes rows k, k+8, ..., in eight independent
 // chains), coalesced 128-byte row segments, and warp 0 adds the 8 subtotals
-// in order.  The order of every
-// addition is fixed by (G, N), so dW / dB are bit-identical from run to run.
+// in order; the cluster form below serves many partial rows.  The order of
+// every addition is fixed by (G, N), so dW / dB are bit-identical from run to
+// run.
 // With G = 0 (no rows) the outputs are set to zero.
+#include <cooperative_groups.h>
+
 #include "launch.h"
 
 namespace gb300norm {
@@ -53,8 +56,92 @@ __global__ void __launch_bounds__(256) colreduce_kernel(const float* __restrict_
   }
 }
 
+// The form for many partial rows (G >= kCrClusterRows, N % 4 == 0: every
+// partial row then starts on a 16-byte boundary, as the workspace is 16-byte
+// aligned and the dB partials start G * N floats after the dW ones).  A
+// thread-block cluster of kCrCluster CTAs owns 128 adjacent columns (lane l:
+// columns 4l..4l+3, 16-byte loads) and splits the G partial rows among its
+// kCrCluster x 8 warps: warp w of CTA r takes rows (8r + w) + 8 kCrCluster i,
+// i = 0, 1, ..., in four independent chains (i mod 4) joined as
+// (c0 + c1) + (c2 + c3).  Each CTA adds its warps' sums in warp order; CTA 0
+// of the cluster adds the CTAs' sums in rank order, read through distributed
+// shared memory, and writes the 128 outputs.  The order of every addition is
+// fixed by (G, N).  With hundreds of partial rows the scalar form's eight
+// chains per warp become a long series of dependent load rounds; the cluster
+// spreads them over 8x the warps.  With fewer rows its fixed cost (cluster
+// launch and barriers) does not pay.
+constexpr int kCrCluster = 8;
+constexpr int kCrClusterRows = 512;
+
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+  const float2 lo = fadd2(make_float2(a.x, a.y), make_float2(b.x, b.y));
+  const float2 hi = fadd2(make_float2(a.z, a.w), make_float2(b.z, b.w));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
+template <class TO>
+__global__ void __cluster_dims__(kCrCluster, 1, 1) __launch_bounds__(256)
+    colreduce_cluster_kernel(const float* __restrict__ ws0, TO* __restrict__ out0, const float* __restrict__ ws1,
+                             TO* __restrict__ out1, int G, int N) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int tile = blockIdx.x / kCrCluster;
+  const float* ws = blockIdx.y ? ws1 : ws0;
+  TO* out = blockIdx.y ? out1 : out0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int col = tile * 128 + lane * 4;
+  __shared__ float4 part[8][32];
+  __shared__ float4 csum[32];
+  // The partial rows come from the row kernel launched just before on this
+  // stream; wait until that grid has completed and its writes are visible.
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 a[4] = {z, z, z, z};
+  if (col < N) {
+    constexpr int W = 8 * kCrCluster;   // warps of the cluster
+    const float4* base = reinterpret_cast<const float4*>(ws + col);
+    const int64_t rs = N / 4;           // row stride in float4
+    int g = rank * 8 + warp;
+    for (; g + 3 * W < G; g += 4 * W) {
+      float4 t[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) t[u] = base[(int64_t)(g + u * W) * rs];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) a[u] = add4(a[u], t[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (g + u * W < G) a[u] = add4(a[u], base[(int64_t)(g + u * W) * rs]);
+    }
+  }
+  part[warp][lane] = add4(add4(a[0], a[1]), add4(a[2], a[3]));
+  __syncthreads();
+  if (warp == 0) {
+    float4 s = part[0][lane];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) s = add4(s, part[w][lane]);
+    csum[lane] = s;
+  }
+  cluster.sync();   // every CTA's csum written and visible to the cluster
+  if (rank == 0 && warp == 0 && col < N) {
+    float4 s = csum[lane];
+#pragma unroll
+    for (int r = 1; r < kCrCluster; ++r) s = add4(s, cluster.map_shared_rank(csum, r)[lane]);
+    out[col] = from_f<TO>(s.x);
+    out[col + 1] = from_f<TO>(s.y);
+    out[col + 2] = from_f<TO>(s.z);
+    out[col + 3] = from_f<TO>(s.w);
+  }
+  cluster.sync();   // the other CTAs keep their shared memory until CTA 0 has read it
+}
+
 template <class TO>
 static int launch_cr(const float* a, void* da, const float* b, void* db, int G, int N, cudaStream_t st) {
+  if (G >= kCrClusterRows && N % 4 == 0)
+    return launch_pdl(colreduce_cluster_kernel<TO>, dim3((unsigned)((N + 127) / 128 * kCrCluster), db ? 2u : 1u),
+                      dim3(256), 0, st, a, static_cast<TO*>(da), b, static_cast<TO*>(db), G, N);
   return launch_pdl(colreduce_kernel<TO>, dim3((unsigned)((N + 31) / 32), db ? 2u : 1u), dim3(256), 0, st, a,
                     static_cast<TO*>(da), b, static_cast<TO*>(db), G, N);
 }
