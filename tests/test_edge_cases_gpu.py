@@ -188,6 +188,28 @@ def test_weight_gradients_are_deterministic(g):
     assert bits_equal(c["dw"], e["dw"])
 
 
+@pytest.mark.parametrize("M,N", [(8192, 4096), (4096, 64), (8192, 2052)])
+def test_many_partial_rows_column_reduce(g, M, N):
+    """Trainable backwards that leave 512 or more dW partial rows (N % 4 == 0)
+    take the thread-block-cluster column reduce: 608 rows at N = 4096, 1216
+    at N = 64 (one partial 128-column tile) and at N = 2052 (a ragged last
+    tile).  dW and dB match the oracle and repeat bit for bit."""
+    case = si.norm_case(M, N, seed=31, dtype="bfloat16")
+    a = run_rms(g, case, dw_dtype=torch.float32)
+    check_rms(a, case, f"cluster reduce rms {M}x{N}")
+    b = run_rms(g, case, dw_dtype=torch.float32)
+    assert bits_equal(a["dw"], b["dw"])
+    c = run_fadd(g, si.norm_case(M, N, seed=32, dtype="bfloat16", with_bias=False, fused_add=True),
+                 dw_dtype=torch.bfloat16)
+    e = run_fadd(g, si.norm_case(M, N, seed=32, dtype="bfloat16", with_bias=False, fused_add=True),
+                 dw_dtype=torch.bfloat16)
+    assert bits_equal(c["dw"], e["dw"])
+    ln1 = run_ln(g, case, dw_dtype=torch.float32)
+    check_ln(ln1, case, f"cluster reduce ln {M}x{N}")
+    ln2 = run_ln(g, case, dw_dtype=torch.float32)
+    assert bits_equal(ln1["dw"], ln2["dw"]) and bits_equal(ln1["db"], ln2["db"])
+
+
 def test_non_default_stream(g):
     M, N = 1024, 4096
     case = si.norm_case(M, N, seed=10, dtype="bfloat16")
