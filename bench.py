@@ -562,12 +562,21 @@ def shape_table(g, flush_l2, reps=40):
 
 
 def kernel_source_hash():
+    """Hash of the CUDA sources' code: comments and blank space removed, so
+    that only a change to what is compiled invalidates committed counters."""
     import glob
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "row_normalization_rmsnorm_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        if not f.endswith((".cu", ".cuh", ".h")):
+            continue
+        with open(f, encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(os.path.basename(f).encode())
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

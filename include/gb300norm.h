@@ -138,7 +138,10 @@ GB300NORM_API int norm_rms_bwd(const void *dy, int64_t dy_stride,
 
 /*
  * LayerNorm forward ("perf(norm): skip dW/dB ...", Key Changes, layer_norm),
- * biased variance, two passes over the row held on chip.
+ * biased variance.  Never E[x^2] - mean^2: each thread takes sums of its
+ * elements about one of them and the block merges them exactly (the
+ * pairwise update of Chan, Golub and LeVeque), one pass over the row held on
+ * chip.
  *   b may be NULL (no bias); mean and rstd may each be NULL.
  */
 GB300NORM_API int norm_ln_fwd(const void *x, int64_t x_stride,

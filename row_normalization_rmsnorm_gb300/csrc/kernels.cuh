@@ -408,8 +408,9 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
     } else {
       // ---- backward -------------------------------------------------------
       if (!have_stats) {
-        // statistics recomputed from the saved row (same arithmetic as the
-        // forward: two passes for LayerNorm)
+        // statistics recomputed from the saved row (no saved statistics
+        // given): the sum of squares for RMSNorm as in its forward; two
+        // passes, mean then sum((x - mean)^2), for LayerNorm
         float2 acc[H];
 #pragma unroll
         for (int h = 0; h < H; ++h) acc[h] = f2s(0.f);
