@@ -54,6 +54,49 @@ def test_tiny_rows(g, M, N, dtype):
         check_ln(run_ln(g, case), case, f"tiny ln {M}x{N} {dtype}")
 
 
+def hard_rows(N, gen):
+    """Rows against the forward's one-pass statistics (each thread's sums
+    about one of its own elements, merged exactly), FP64: [well-conditioned
+    ones], [ones whose mean is 1e5 / 5e4 times their spread]."""
+    good = []
+    r = torch.randn(N, generator=gen, dtype=torch.float64)
+    r[::4] = 1e4          # the first element of every 16-byte fp32 chunk: every thread's shift
+    good.append(r)
+    r = torch.randn(N, generator=gen, dtype=torch.float64)
+    r[0] = 1e4            # one outlier, thread 0's shift
+    good.append(r)
+    good.append(torch.full((N,), 3.0, dtype=torch.float64))   # zero variance
+    offset = [1000.0 + 0.01 * torch.randn(N, generator=gen, dtype=torch.float64),
+              -50.0 + 1e-3 * torch.randn(N, generator=gen, dtype=torch.float64)]
+    return good, offset
+
+
+@pytest.mark.parametrize("N", [4096, 8192])
+def test_layernorm_statistics_hard_rows(g, N):
+    """FP32 rows built against the forward's one-pass statistics, against the
+    two-pass FP64 oracle.  mean and rstd are checked on every row.  y, dx, dW
+    and dB are checked on the well-conditioned ones.  Where |mean| / spread is
+    1e5, y itself carries the FP32 rounding of the mean, which any FP32
+    statistics share."""
+    gen = torch.Generator().manual_seed(5)
+    good, offset = hard_rows(N, gen)
+    x_all = torch.stack(good + offset).repeat(32, 1).to(torch.float32)
+    M = x_all.shape[0]
+    w = (1 + 0.1 * torch.randn(N, generator=gen)).to(torch.float32)
+    b = (0.1 * torch.randn(N, generator=gen)).to(torch.float32)
+    xd = x_all.cuda()
+    y = torch.empty_like(xd)
+    mean = torch.empty(M, device="cuda")
+    rstd = torch.empty(M, device="cuda")
+    g.norm_ln_fwd(xd, w.cuda(), b.cuda(), y, mean, rstd, 0.0, EPS)
+    _, ref_mean, ref_rstd, _ = oracle.ln_fwd(f64(x_all), f64(w), f64(b), 0.0, EPS)
+    check(mean, ref_mean, "float32", scale=16 * np.abs(f64(x_all)).mean(axis=1), label=f"hard rows mean N={N}")
+    check(rstd, ref_rstd, "float32", label=f"hard rows rstd N={N}")
+    xg = torch.stack(good).repeat(64, 1).to(torch.float32)
+    case = {"x": xg, "dy": torch.randn(xg.shape[0], N, generator=gen).to(torch.float32), "w": w, "b": b}
+    check_ln(run_ln(g, case), case, f"hard rows ln fp32 N={N}")
+
+
 def test_single_element_layernorm_gives_bias(g):
     case = si.norm_case(4, 1, seed=1, dtype="float32")
     out = run_ln(g, case)
