@@ -94,12 +94,22 @@ def _check(fn: str, rc: int):
         raise NormError(fn, rc)
 
 
-def _stream(stream):
+# The current stream's raw handle without building a torch.cuda.Stream object
+# on every call (that alone cost more than the rest of a small call).
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream, like=None):
+    """Raw cudaStream_t (an int) for the C ABI: `stream`, else the current
+    stream of `like`'s device (else of the current device)."""
     if stream is None:
-        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        if _raw_stream is not None:
+            dev = like.get_device() if like is not None else torch.cuda.current_device()
+            return _raw_stream(dev)
+        return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, torch.cuda.Stream):
-        return ctypes.c_void_p(stream.cuda_stream)
-    return ctypes.c_void_p(int(stream))
+        return stream.cuda_stream
+    return int(stream)
 
 
 def _dev(t, name, dims=None):
@@ -110,11 +120,13 @@ def _dev(t, name, dims=None):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor (this library has no CPU path)")
-    if dims is not None and t.dim() != dims:
+    st = t.stride()
+    nd = len(st)
+    if dims is not None and nd != dims:
         raise ValueError(f"{name} must be {dims}-D, got shape {tuple(t.shape)}")
-    if t.dim() == 2 and t.shape[1] > 1 and t.stride(1) != 1:
+    if nd == 2 and st[1] != 1 and t.shape[1] > 1:
         raise ValueError(f"{name} rows must be contiguous (stride(1) == 1)")
-    if t.dim() == 1 and t.numel() > 1 and t.stride(0) != 1:
+    if nd == 1 and st[0] != 1 and t.numel() > 1:
         raise ValueError(f"{name} must be contiguous")
     return t.data_ptr() or None
 
@@ -153,7 +165,7 @@ def norm_rms_fwd(x, w, y, rstd=None, offset=0.0, eps=1e-6, stream=None):
     M, N = x.shape
     rc = lib.norm_rms_fwd(_dev(x, "x", 2), _rs(x), _dev(w, "w", 1), _dev(y, "y", 2), _rs(y),
                           _dev(rstd, "rstd", 1), M, N, float(offset), float(eps),
-                          DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream))
+                          DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream, x))
     _check("norm_rms_fwd", rc)
 
 
@@ -165,7 +177,7 @@ def norm_rms_bwd(dy, x, w, rstd, dx, dw=None, workspace=None, offset=0.0, eps=1e
                           _dev(rstd, "rstd", 1), _dev(dx, "dx", 2), _rs(dx),
                           _dev(dw, "dw", 1), DTYPE_CODE[dw.dtype] if dw is not None else NORM_F32,
                           _dev(workspace, "workspace"), ws_bytes, M, N, float(offset), float(eps),
-                          DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream))
+                          DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream, x))
     _check("norm_rms_bwd", rc)
 
 
@@ -176,7 +188,7 @@ def norm_rms_bwd_noalloc(dy, x, w, rstd, dx, dw=None, offset=0.0, eps=1e-6, stre
     rc = lib.norm_rms_bwd_noalloc(_dev(dy, "dy", 2), _rs(dy), _dev(x, "x", 2), _rs(x), _dev(w, "w", 1),
                                   _dev(rstd, "rstd", 1), _dev(dx, "dx", 2), _rs(dx), _dev(dw, "dw", 1),
                                   DTYPE_CODE[dw.dtype] if dw is not None else NORM_F32, M, N, float(offset),
-                                  float(eps), DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream))
+                                  float(eps), DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream, x))
     _check("norm_rms_bwd_noalloc", rc)
 
 
@@ -185,7 +197,7 @@ def norm_ln_fwd(x, w, b, y, mean=None, rstd=None, offset=0.0, eps=1e-6, stream=N
     M, N = x.shape
     rc = lib.norm_ln_fwd(_dev(x, "x", 2), _rs(x), _dev(w, "w", 1), _dev(b, "b", 1), _dev(y, "y", 2), _rs(y),
                          _dev(mean, "mean", 1), _dev(rstd, "rstd", 1), M, N, float(offset), float(eps),
-                         DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream))
+                         DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream, x))
     _check("norm_ln_fwd", rc)
 
 
@@ -200,7 +212,7 @@ def norm_ln_bwd(dy, x, w, mean, rstd, dx, dw=None, db=None, workspace=None, offs
                          _dev(dw, "dw", 1), _dev(db, "db", 1),
                          DTYPE_CODE[gd.dtype] if gd is not None else NORM_F32,
                          _dev(workspace, "workspace"), ws_bytes, M, N, float(offset), float(eps),
-                         DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream))
+                         DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream, x))
     _check("norm_ln_bwd", rc)
 
 
@@ -210,7 +222,7 @@ def norm_fused_add_rms_fwd(x, residual, w, y, h_out, rstd=None, offset=0.0, eps=
     rc = lib.norm_fused_add_rms_fwd(_dev(x, "x", 2), _rs(x), _dev(residual, "residual", 2), _rs(residual),
                                     _dev(w, "w", 1), _dev(y, "y", 2), _rs(y), _dev(h_out, "h_out", 2),
                                     _rs(h_out), _dev(rstd, "rstd", 1), M, N, float(offset), float(eps),
-                                    DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream))
+                                    DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream, x))
     _check("norm_fused_add_rms_fwd", rc)
 
 
@@ -224,5 +236,5 @@ def norm_fused_add_rms_bwd(dy, dh_out, h, w, rstd, dx, dw=None, workspace=None, 
                                     _dev(dx, "dx", 2), _rs(dx), _dev(dw, "dw", 1),
                                     DTYPE_CODE[dw.dtype] if dw is not None else NORM_F32,
                                     _dev(workspace, "workspace"), ws_bytes, M, N, float(offset), float(eps),
-                                    DTYPE_CODE[h.dtype], DTYPE_CODE[w.dtype], _stream(stream))
+                                    DTYPE_CODE[h.dtype], DTYPE_CODE[w.dtype], _stream(stream, h))
     _check("norm_fused_add_rms_bwd", rc)
