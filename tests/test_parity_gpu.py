@@ -231,6 +231,17 @@ def test_config3_gemma_rms_bf16(g, M, N):
     check_rms(run_rms(g, case, offset=1.0), case, f"gemma bf16 {M}x{N}", offset=1.0)
 
 
+@pytest.mark.parametrize("wdtype", [None, "float32"])
+@pytest.mark.parametrize("M,N", [(128, 4096), (2048, 8192)])
+def test_gemma_fp16(g, M, N, wdtype):
+    """fp16 activations with the Gemma offset added in FP32 (w = 0.01 N(0,1),
+    offset 1): RMSNorm and FusedAddRMSNorm, fp16 or fp32 weights."""
+    case = si.norm_case(M, N, seed=7, dtype="float16", w_dtype=wdtype, gemma=True, with_bias=False)
+    check_rms(run_rms(g, case, offset=1.0), case, f"gemma fp16/{wdtype or 'fp16'} {M}x{N}", offset=1.0)
+    fcase = si.norm_case(M, N, seed=8, dtype="float16", w_dtype=wdtype, gemma=True, with_bias=False, fused_add=True)
+    check_fadd(run_fadd(g, fcase, offset=1.0), fcase, f"gemma fadd fp16/{wdtype or 'fp16'} {M}x{N}", offset=1.0)
+
+
 def test_gemma_repro_error_magnitudes(g):
     """The minimal reproduction's setting (M=128, N=4096, seed 42, weight
     scale 0.01, offset 1): the distance to the correctly rounded result is
