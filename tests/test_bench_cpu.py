@@ -1,0 +1,78 @@
+"""Host-side checks of bench.py (no GPU): the reference arm's JSON line, the
+algorithmic byte counts behind every GB/s figure, the shape grid, and the
+source hash that guards committed ncu counters."""
+import json
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_algorithmic_bytes_at_8192():
+    # reads of x, dy, residual, w (and bias), rstd (and mean), writes of y,
+    # dx, h_out and dW (dB) -- bf16 tensors, FP32 statistics
+    M = N = 8192
+    MN = M * N
+    assert bench.op_bytes("rms_fwd", M, N) == 2 * MN * 2 + N * 2 + 4 * M == 268484608
+    assert bench.op_bytes("ln_fwd", M, N) == 2 * MN * 2 + 2 * N * 2 + 8 * M == 268533760
+    assert bench.op_bytes("fadd_fwd", M, N) == 4 * MN * 2 + N * 2 + 4 * M == 536920064
+    assert bench.op_bytes("rms_bwd", M, N) == 402718720
+    assert bench.op_bytes("rms_bwd", M, N, trainable=False) == 402718720 - N * 2
+    assert bench.op_bytes("ln_bwd", M, N) == 402767872
+    assert bench.op_bytes("ln_bwd", M, N, trainable=False) == 402767872 - 2 * N * 2
+    assert bench.op_bytes("fadd_bwd", M, N) == 536936448
+    with pytest.raises(ValueError):
+        bench.op_bytes("softmax", M, N)
+
+
+def test_grid_covers_the_configured_shapes():
+    fams = bench.grid_families()
+    for sh in bench.GRID_SHAPES:
+        assert {"rms", "ln"} <= set(fams[sh])
+    for sh in bench.FADD_SHAPES + [(8192, 8192)]:
+        assert "fadd" in fams[sh]
+    for sh in bench.GEMMA_SHAPES:
+        assert "rms" in fams[sh]
+    assert all(len(set(v)) == len(v) for v in fams.values())   # no family twice
+
+
+def test_source_hash_ignores_comments(tmp_path):
+    src = os.path.join(ROOT, "row_normalization_rmsnorm_gb300", "csrc")
+    pkg = tmp_path / "row_normalization_rmsnorm_gb300"
+    shutil.copytree(src, pkg / "csrc")
+    old_root = bench.ROOT
+    try:
+        bench.ROOT = str(tmp_path)
+        h0 = bench.kernel_source_hash()
+        f = pkg / "csrc" / "colreduce.cu"
+        text = f.read_text()
+        f.write_text("// a comment line\n" + text.replace("\n\n", "\n\n/* a block\n comment */\n", 1))
+        assert bench.kernel_source_hash() == h0
+        f.write_text(text.replace("kCrClusterRows = 512", "kCrClusterRows = 513"))
+        assert bench.kernel_source_hash() != h0
+    finally:
+        bench.ROOT = old_root
+
+
+def test_reference_arm_prints_one_contract_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2",
+                          "--warmup", "1", "--M", "64", "--N", "512", "--ref-rows", "16"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT, check=True)
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    assert j["impl"] == "reference"
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in j, key
+    assert j["metric"] == bench.METRIC and j["unit"] == "GB/s" and j["higher_is_better"] is True
+    assert j["steps"] == 2 and j["warmup"] == 1 and j["value"] > 0
+    assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["value"] == j["value"]
+    assert j["e2e"] == {"value": j["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
