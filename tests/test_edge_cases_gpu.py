@@ -231,12 +231,14 @@ def test_weight_gradients_are_deterministic(g):
     assert bits_equal(c["dw"], e["dw"])
 
 
-@pytest.mark.parametrize("M,N", [(8192, 4096), (4096, 64), (8192, 2052)])
+@pytest.mark.parametrize("M,N", [(8192, 4096), (4096, 64), (8192, 2052), (4096, 4095)])
 def test_many_partial_rows_column_reduce(g, M, N):
-    """Trainable backwards that leave 512 or more dW partial rows (N % 4 == 0)
-    take the thread-block-cluster column reduce: 608 rows at N = 4096, 1216
-    at N = 64 (one partial 128-column tile) and at N = 2052 (a ragged last
-    tile).  dW and dB match the oracle and repeat bit for bit."""
+    """Trainable backwards that leave 512 or more dW partial rows take the
+    thread-block-cluster column reduce when N % 4 == 0: 608 rows at N = 4096,
+    1216 at N = 64 (one partial 128-column tile) and at N = 2052 (a ragged
+    last tile).  N = 4095 (general row kernel, partial rows not 16-byte
+    aligned) keeps the scalar reduce.  dW and dB match the oracle and repeat
+    bit for bit."""
     case = si.norm_case(M, N, seed=31, dtype="bfloat16")
     a = run_rms(g, case, dw_dtype=torch.float32)
     check_rms(a, case, f"cluster reduce rms {M}x{N}")
