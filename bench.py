@@ -18,12 +18,17 @@ Reported (one JSON line on rank 0):
   per_op       the same for every operation, trainable and frozen;
   e2e          the same metric with host buffers: pinned host -> device copies
                of every input and device -> host copies of every output inside
-               the timed region, through the same C-ABI calls;
+               the timed region, through the same C-ABI calls (downloads on a
+               second stream, overlapping the next upload);
+  shapes       per-call times (one call at a time, clean L2) on the pages'
+               shape grid, Gemma and FusedAdd shapes;
   cpu_baseline the FP64 CPU oracle on a bounded row sample of the same
                workload, on this host's cores (a reported baseline).
 
 --impl reference times that oracle alone (the pages give no runnable
 reference implementation), on the same metric and workload.
+--grid runs every operation of the shape grid twice, untimed, for an ncu
+kernel-duration capture, and prints the call order.
 """
 from __future__ import annotations
 
