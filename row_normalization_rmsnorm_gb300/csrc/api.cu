@@ -97,6 +97,9 @@ int check_mat(const Mat& m, int64_t M, int64_t N, int es, bool required) {
   if (M == 0) return NORM_OK;
   if (!m.p) return required ? NORM_ERR_NULL : NORM_OK;
   if (m.stride < N) return NORM_ERR_STRIDE;
+  // the byte extent ((M - 1) * stride + N) * es must fit in 63 bits (it is
+  // formed on the host for the overlap checks and in the kernels' row offsets)
+  if (M - 1 > (INT64_MAX / es - N) / m.stride) return NORM_ERR_SHAPE;
   if (reinterpret_cast<uintptr_t>(m.p) % (uintptr_t)es) return NORM_ERR_ALIGN;
   return NORM_OK;
 }

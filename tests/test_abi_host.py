@@ -85,6 +85,7 @@ def rms_bwd(g, **kw):
     (dict(x=X + 1), 6), (dict(w=W + 1), 6), (dict(rstd=R + 2), 6),
     (dict(eps=-1e-6), 7), (dict(eps=float("inf")), 7), (dict(off=float("nan")), 7),
     (dict(y=X + 2 * 64, ys=64), 8), (dict(rstd=X + 8), 8), (dict(y=W), 8),
+    (dict(M=1 << 40, xs=1 << 30, ys=1 << 30), 2),   # byte extent beyond 63 bits
 ])
 def test_rms_fwd_argument_errors(g, kw, code):
     assert rms_fwd(g, **kw) == code
