@@ -68,8 +68,8 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
   constexpr bool LN = (OP == LN_FWD || OP == LN_BWD);
   constexpr bool BWD = OpInfo<OP>::BWD;
   // Up to 4 chunks per thread, W' (and the bias) live in registers; at 8
-  // (rows of 2049-4096 chunks) they move to shared memory to leave the
-  // registers to the dW / dB accumulators.
+  // (the only staged shape for rows of 2049-4096 chunks) they move to shared
+  // memory to leave the registers to the dW / dB accumulators.
   constexpr bool WREG = staged_wreg(NPT);
   // The FusedAdd forward keeps its FP32 row h in registers between passes
   // (up to 4 chunks per thread); RMSNorm and LayerNorm re-read theirs from
