@@ -225,45 +225,95 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU oracle baseline
 # ---------------------------------------------------------------------------
-def oracle_step(host, rows):
-    """Run the oracle on the first `rows` rows of every operation's inputs.
-    Returns (seconds, algorithmic bytes of that sample)."""
-    import oracle
-    f = lambda t: t[:rows].double().numpy()  # noqa: E731
+def host_cores():
+    """Threads this process may run on (its CPU affinity)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_blocks(host, rows, nblocks):
+    """FP64 copies of the first `rows` rows of every operation's inputs, cut
+    into `nblocks` contiguous row blocks (prepared outside any timed region)."""
+    f = lambda t: np.ascontiguousarray(t[:rows].double().numpy())  # noqa: E731
     w = {k: host[k]["w"].double().numpy() for k in host}
     rms, ln, fa = host["rms"], host["ln"], host["fadd"]
-    a = dict(rx=f(rms["x"]), rdy=f(rms["dy"]), lx=f(ln["x"]), ldy=f(ln["dy"]), lb=ln["b"].double().numpy(),
-             fx=f(fa["x"]), fr=f(fa["residual"]), fdy=f(fa["dy"]), fdh=f(fa["dh_out"]))
-    N = a["rx"].shape[1]
-    t0 = time.perf_counter()
+    full = dict(rx=f(rms["x"]), rdy=f(rms["dy"]), lx=f(ln["x"]), ldy=f(ln["dy"]),
+                fx=f(fa["x"]), fr=f(fa["residual"]), fdy=f(fa["dy"]), fdh=f(fa["dh_out"]))
+    cuts = np.linspace(0, rows, nblocks + 1).astype(int)
+    blocks = [{k: np.ascontiguousarray(v[lo:hi]) for k, v in full.items()}
+              for lo, hi in zip(cuts[:-1], cuts[1:]) if hi > lo]
+    return blocks, w, ln["b"].double().numpy()
+
+
+def oracle_block(a, w, lb):
+    """The six operations of one step on one row block; returns the block's
+    dW / dB partial sums (the column reduction over its rows)."""
+    import oracle
     oracle.rms_fwd(a["rx"], w["rms"], 0.0, 1e-6)
-    oracle.ln_fwd(a["lx"], w["ln"], a["lb"], 0.0, 1e-6)
+    oracle.ln_fwd(a["lx"], w["ln"], lb, 0.0, 1e-6)
     _, h, _ = oracle.fused_add_rms_fwd(a["fx"], a["fr"], w["fadd"], 0.0, 1e-6)
-    oracle.rms_bwd(a["rx"], a["rdy"], w["rms"], 0.0, 1e-6)
-    oracle.ln_bwd(a["lx"], a["ldy"], w["ln"], 0.0, 1e-6)
-    oracle.fused_add_rms_bwd(h, a["fdy"], w["fadd"], a["fdh"], 0.0, 1e-6)
+    _, dw_r, _ = oracle.rms_bwd(a["rx"], a["rdy"], w["rms"], 0.0, 1e-6)
+    _, dw_l, db_l, _ = oracle.ln_bwd(a["lx"], a["ldy"], w["ln"], 0.0, 1e-6)
+    _, dw_f, _ = oracle.fused_add_rms_bwd(h, a["fdy"], w["fadd"], a["fdh"], 0.0, 1e-6)
+    return dw_r, dw_l, db_l, dw_f
+
+
+def oracle_step(host, rows, threads=1, prepared=None):
+    """Run the oracle on the first `rows` rows of every operation's inputs,
+    split into `threads` row blocks run concurrently (the oracle's C calls
+    release the interpreter lock); the blocks' dW / dB partial sums are added
+    in block order.  Returns (seconds, algorithmic bytes of that sample)."""
+    from concurrent.futures import ThreadPoolExecutor
+    blocks, w, lb = prepared or oracle_blocks(host, rows, threads)
+    N = blocks[0]["rx"].shape[1]
+    t0 = time.perf_counter()
+    if len(blocks) == 1:
+        parts = [oracle_block(blocks[0], w, lb)]
+    else:
+        with ThreadPoolExecutor(len(blocks)) as ex:
+            parts = list(ex.map(lambda a: oracle_block(a, w, lb), blocks))
+    total = [p.copy() for p in parts[0]]
+    for p in parts[1:]:
+        for t, q in zip(total, p):
+            t += q
     dt = time.perf_counter() - t0
     return dt, sum(op_bytes(op, rows, N) for op in OPS)
 
 
-def cpu_baseline(host, target_s=10.0):
-    """The oracle on `rows` rows of every operation, repeated until about
-    target_s seconds of CPU time have been spent."""
+def timed_oracle(host, threads, target_s):
+    """GB/s of the oracle on `threads` threads: a row sample sized to about
+    target_s seconds, repeated until target_s has passed."""
     import oracle
     oracle.build()
     M = host["rms"]["x"].shape[0]
-    rows = min(M, 16)
-    dt, _ = oracle_step(host, rows)
-    rows = int(min(M, max(16, rows * target_s / max(dt, 1e-3))))
+    rows = min(M, 16 * threads)
+    dt, _ = oracle_step(host, rows, threads)
+    rows = int(min(M, max(16 * threads, rows * (target_s / 2) / max(dt, 1e-3))))
+    prepared = oracle_blocks(host, rows, threads)
     total, nbytes, reps = 0.0, 0, 0
     while total < target_s or reps == 0:
-        dt, b = oracle_step(host, rows)
+        dt, b = oracle_step(host, rows, threads, prepared)
         total += dt
         nbytes += b
         reps += 1
-    return {"value": nbytes / total / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{rows} rows of each of the 6 operations at N={host['rms']['x'].shape[1]}, "
-                      f"{reps} repetition(s), {total:.1f} s (single-threaded FP64 C oracle)"}
+    return nbytes / total / 1e9, rows, reps, total
+
+
+def cpu_baseline(host, target_s=10.0):
+    """The FP64 oracle on a row sample of the same workload, on every core of
+    this host (one thread per core, each on its own row block), with the
+    single-thread figure beside it."""
+    cores = host_cores()
+    v, rows, reps, total = timed_oracle(host, cores, target_s)
+    v1, rows1, _, total1 = timed_oracle(host, 1, target_s / 3)
+    N = host["rms"]["x"].shape[1]
+    return {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "single_thread_value": v1,
+            "sample": f"{rows} rows of each of the 6 operations at N={N} in {cores} row blocks on {cores} threads, "
+                      f"{reps} repetition(s), {total:.1f} s (FP64 C oracle; dW/dB block partials added in block "
+                      f"order); single thread: {rows1} rows, {total1:.1f} s"}
 
 
 # ---------------------------------------------------------------------------
@@ -284,12 +334,14 @@ def run_reference(args):
     host = host_inputs(M, N, seed=0)
     import oracle
     oracle.build()
-    rows = args.ref_rows
+    cores = host_cores()
+    rows = max(args.ref_rows, 16 * cores)
+    prepared = oracle_blocks(host, rows, cores)
     for _ in range(args.warmup):
-        oracle_step(host, rows)
+        oracle_step(host, rows, cores, prepared)
     times, nbytes = [], 0
     for _ in range(args.steps):
-        dt, nbytes = oracle_step(host, rows)
+        dt, nbytes = oracle_step(host, rows, cores, prepared)
         times.append(dt)
     total = sum(times)
     value = nbytes * args.steps / total / 1e9
@@ -300,8 +352,9 @@ def run_reference(args):
         "data": "synthetic",
         "config": {"workload": f"bf16 {M}x{N} RMSNorm+LayerNorm+FusedAddRMSNorm fwd+bwd (trainable)",
                    "M": M, "N": N, "sample_rows": rows},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{rows} rows of each of the 6 operations per step"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} rows of each of the 6 operations per step, in {cores} row blocks "
+                                   f"on {cores} threads"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -1,10 +1,16 @@
 """ctypes binding of libgb300norm.so (the C ABI in include/gb300norm.h).
 
-Argument marshalling only: every function below takes torch tensors that
-already live on the current CUDA device, passes their data pointers, row
-strides, shapes and dtype codes to the C entry point of the same name and
-raises NormError on a non-zero status.  Nothing is computed here and there is
-no CPU path: a CPU tensor, or a missing library, is an error.
+Argument marshalling only: every function below takes torch tensors on one
+CUDA device, passes their data pointers, row strides, shapes and dtype codes
+to the C entry point of the same name (with that device current) and raises
+NormError on a non-zero status.  Nothing is computed here and there is no
+CPU path: a CPU tensor, or a missing library, is an error.
+
+The C ABI sees only pointers, so the extent of every buffer is checked here
+before the call: each 2-D tensor must be (M, N) in the activation dtype with
+contiguous rows, w / b / dW / dB must hold N elements, rstd / mean at least
+M FP32 values, and every tensor must sit on x's device.  Shape and dtype
+errors raise ValueError (before any device check), a CPU tensor TypeError.
 """
 from __future__ import annotations
 
@@ -112,23 +118,99 @@ def _stream(stream, like=None):
     return int(stream)
 
 
-def _dev(t, name, dims=None):
-    """Data pointer of a CUDA tensor (or None), checked for device and layout."""
-    if t is None:
-        return None
+def _tensor(t, name):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
-        raise TypeError(f"{name} must be a CUDA tensor (this library has no CPU path)")
-    st = t.stride()
-    nd = len(st)
-    if dims is not None and nd != dims:
-        raise ValueError(f"{name} must be {dims}-D, got shape {tuple(t.shape)}")
-    if nd == 2 and st[1] != 1 and t.shape[1] > 1:
+    return t
+
+
+def _mat(t, name, M, N, dtype, required=True):
+    """Check a 2-D row tensor: shape (M, N), the activation dtype, rows
+    contiguous.  Runs before any device check, so a shape error is reported
+    as such whatever the tensor's device."""
+    if t is None:
+        if required:
+            raise ValueError(f"{name} is required")
+        return
+    _tensor(t, name)
+    if t.dim() != 2 or tuple(t.shape) != (M, N):
+        raise ValueError(f"{name} must have shape ({M}, {N}), got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if M > 0 and N > 1 and t.stride(1) != 1:
         raise ValueError(f"{name} rows must be contiguous (stride(1) == 1)")
-    if nd == 1 and st[0] != 1 and t.numel() > 1:
+
+
+def _vec(t, name, n, dtypes, at_least=False, required=True):
+    """Check a 1-D contiguous vector of n elements (at least n when
+    `at_least`) whose dtype is one of `dtypes`."""
+    if t is None:
+        if required:
+            raise ValueError(f"{name} is required")
+        return
+    _tensor(t, name)
+    if t.dim() != 1:
+        raise ValueError(f"{name} must be 1-D, got shape {tuple(t.shape)}")
+    if (t.numel() < n) if at_least else (t.numel() != n):
+        raise ValueError(f"{name} must have {'at least ' if at_least else ''}{n} elements, got {t.numel()}")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} must be one of {[str(d) for d in dtypes]}, got {t.dtype}")
+    if t.numel() > 1 and t.stride(0) != 1:
         raise ValueError(f"{name} must be contiguous")
-    return t.data_ptr() or None
+
+
+def _act_dtype(x, name="x"):
+    _tensor(x, name)
+    if x.dim() != 2:
+        raise ValueError(f"{name} must be 2-D [M, N], got shape {tuple(x.shape)}")
+    if x.dtype not in DTYPE_CODE:
+        raise ValueError(f"{name} dtype {x.dtype} is not supported")
+    return x.dtype
+
+
+def _weight(w, N):
+    _tensor(w, "w")
+    _vec(w, "w", N, tuple(DTYPE_CODE))
+    return w.dtype
+
+
+def _grad_dtype(w_dtype, *grads):
+    """dtype code of the dW / dB outputs: FP32 or the weight's dtype, the
+    same for every gradient given."""
+    given = [(n, t) for n, t in grads if t is not None]
+    if not given:
+        return NORM_F32
+    dt = given[0][1].dtype
+    if dt not in (torch.float32, w_dtype):
+        raise ValueError(f"{given[0][0]} must be float32 or the weight dtype {w_dtype}, got {dt}")
+    for n, t in given[1:]:
+        if t.dtype != dt:
+            raise ValueError(f"{n} must have the same dtype as {given[0][0]} ({dt}), got {t.dtype}")
+    return DTYPE_CODE[dt]
+
+
+def _device(x, *others):
+    """Index of the CUDA device every tensor lives on (x's), or an error."""
+    if not x.is_cuda:
+        raise TypeError("x must be a CUDA tensor (this library has no CPU path)")
+    dev = x.get_device()
+    for name, t in others:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor (this library has no CPU path)")
+        if t.get_device() != dev:
+            raise ValueError(f"{name} is on cuda:{t.get_device()}, x on cuda:{dev}")
+    return dev
+
+
+def _on(dev, fn):
+    """Run fn with `dev` as the current device: the C ABI takes its device
+    (launch shapes, status word) from the current device."""
+    if dev == torch.cuda.current_device():
+        return fn()
+    with torch.cuda.device(dev):
+        return fn()
 
 
 def _rs(t):
@@ -137,6 +219,15 @@ def _rs(t):
 
 def _ptr(t):
     return None if t is None else (t.data_ptr() or None)
+
+
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    _tensor(workspace, "workspace")
+    if not workspace.is_contiguous():
+        raise ValueError("workspace must be contiguous")
+    return workspace.data_ptr() or None, workspace.numel() * workspace.element_size()
 
 
 def norm_bwd_workspace_bytes(M: int, N: int, has_dw: bool, has_db: bool = False) -> int:
@@ -160,81 +251,124 @@ def norm_debug_tune(key: int, value: int):
     _check("norm_debug_tune", lib.norm_debug_tune(int(key), int(value)))
 
 
+_F32 = (torch.float32,)
+
+
 def norm_rms_fwd(x, w, y, rstd=None, offset=0.0, eps=1e-6, stream=None):
     """y = RMSNorm(x) with scale (w + offset); rstd (FP32, [M]) optional."""
+    dt = _act_dtype(x)
     M, N = x.shape
-    rc = lib.norm_rms_fwd(_dev(x, "x", 2), _rs(x), _dev(w, "w", 1), _dev(y, "y", 2), _rs(y),
-                          _dev(rstd, "rstd", 1), M, N, float(offset), float(eps),
-                          DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream, x))
-    _check("norm_rms_fwd", rc)
+    wdt = _weight(w, N)
+    _mat(y, "y", M, N, dt)
+    _vec(rstd, "rstd", M, _F32, at_least=True, required=False)
+    dev = _device(x, ("w", w), ("y", y), ("rstd", rstd))
+    _on(dev, lambda: _check("norm_rms_fwd", lib.norm_rms_fwd(
+        _ptr(x), _rs(x), _ptr(w), _ptr(y), _rs(y), _ptr(rstd), M, N, float(offset), float(eps),
+        DTYPE_CODE[dt], DTYPE_CODE[wdt], _stream(stream, x))))
+
+
+def _rms_bwd_checks(dy, x, w, rstd, dx, dw):
+    dt = _act_dtype(x)
+    M, N = x.shape
+    wdt = _weight(w, N)
+    _mat(dy, "dy", M, N, dt)
+    _mat(dx, "dx", M, N, dt)
+    _vec(rstd, "rstd", M, _F32, at_least=True, required=False)
+    _vec(dw, "dw", N, (torch.float32, wdt), required=False)
+    dwt = _grad_dtype(wdt, ("dw", dw))
+    dev = _device(x, ("dy", dy), ("w", w), ("rstd", rstd), ("dx", dx), ("dw", dw))
+    return dt, wdt, dwt, dev
 
 
 def norm_rms_bwd(dy, x, w, rstd, dx, dw=None, workspace=None, offset=0.0, eps=1e-6, stream=None):
     """dx (and dw unless None = frozen) of RMSNorm; rstd None = recompute."""
+    dt, wdt, dwt, dev = _rms_bwd_checks(dy, x, w, rstd, dx, dw)
     M, N = x.shape
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib.norm_rms_bwd(_dev(dy, "dy", 2), _rs(dy), _dev(x, "x", 2), _rs(x), _dev(w, "w", 1),
-                          _dev(rstd, "rstd", 1), _dev(dx, "dx", 2), _rs(dx),
-                          _dev(dw, "dw", 1), DTYPE_CODE[dw.dtype] if dw is not None else NORM_F32,
-                          _dev(workspace, "workspace"), ws_bytes, M, N, float(offset), float(eps),
-                          DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream, x))
-    _check("norm_rms_bwd", rc)
+    _device(x, ("workspace", workspace))
+    wsp, wsb = _ws(workspace)
+    _on(dev, lambda: _check("norm_rms_bwd", lib.norm_rms_bwd(
+        _ptr(dy), _rs(dy), _ptr(x), _rs(x), _ptr(w), _ptr(rstd), _ptr(dx), _rs(dx), _ptr(dw), dwt, wsp, wsb,
+        M, N, float(offset), float(eps), DTYPE_CODE[dt], DTYPE_CODE[wdt], _stream(stream, x))))
 
 
 def norm_rms_bwd_noalloc(dy, x, w, rstd, dx, dw=None, offset=0.0, eps=1e-6, stream=None):
     """norm_rms_bwd without a workspace: the dW partial sums use the
     library's fixed scratch (for callers that cannot allocate)."""
+    dt, wdt, dwt, dev = _rms_bwd_checks(dy, x, w, rstd, dx, dw)
     M, N = x.shape
-    rc = lib.norm_rms_bwd_noalloc(_dev(dy, "dy", 2), _rs(dy), _dev(x, "x", 2), _rs(x), _dev(w, "w", 1),
-                                  _dev(rstd, "rstd", 1), _dev(dx, "dx", 2), _rs(dx), _dev(dw, "dw", 1),
-                                  DTYPE_CODE[dw.dtype] if dw is not None else NORM_F32, M, N, float(offset),
-                                  float(eps), DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream, x))
-    _check("norm_rms_bwd_noalloc", rc)
+    _on(dev, lambda: _check("norm_rms_bwd_noalloc", lib.norm_rms_bwd_noalloc(
+        _ptr(dy), _rs(dy), _ptr(x), _rs(x), _ptr(w), _ptr(rstd), _ptr(dx), _rs(dx), _ptr(dw), dwt, M, N,
+        float(offset), float(eps), DTYPE_CODE[dt], DTYPE_CODE[wdt], _stream(stream, x))))
 
 
 def norm_ln_fwd(x, w, b, y, mean=None, rstd=None, offset=0.0, eps=1e-6, stream=None):
     """y = LayerNorm(x) with scale (w + offset) and bias b (None = no bias)."""
+    dt = _act_dtype(x)
     M, N = x.shape
-    rc = lib.norm_ln_fwd(_dev(x, "x", 2), _rs(x), _dev(w, "w", 1), _dev(b, "b", 1), _dev(y, "y", 2), _rs(y),
-                         _dev(mean, "mean", 1), _dev(rstd, "rstd", 1), M, N, float(offset), float(eps),
-                         DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream, x))
-    _check("norm_ln_fwd", rc)
+    wdt = _weight(w, N)
+    _vec(b, "b", N, (wdt,), required=False)
+    _mat(y, "y", M, N, dt)
+    _vec(mean, "mean", M, _F32, at_least=True, required=False)
+    _vec(rstd, "rstd", M, _F32, at_least=True, required=False)
+    dev = _device(x, ("w", w), ("b", b), ("y", y), ("mean", mean), ("rstd", rstd))
+    _on(dev, lambda: _check("norm_ln_fwd", lib.norm_ln_fwd(
+        _ptr(x), _rs(x), _ptr(w), _ptr(b), _ptr(y), _rs(y), _ptr(mean), _ptr(rstd), M, N, float(offset),
+        float(eps), DTYPE_CODE[dt], DTYPE_CODE[wdt], _stream(stream, x))))
 
 
 def norm_ln_bwd(dy, x, w, mean, rstd, dx, dw=None, db=None, workspace=None, offset=0.0, eps=1e-6,
                 stream=None):
     """dx, and dw / db unless None (frozen), of LayerNorm."""
+    dt = _act_dtype(x)
     M, N = x.shape
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    gd = dw if dw is not None else db
-    rc = lib.norm_ln_bwd(_dev(dy, "dy", 2), _rs(dy), _dev(x, "x", 2), _rs(x), _dev(w, "w", 1),
-                         _dev(mean, "mean", 1), _dev(rstd, "rstd", 1), _dev(dx, "dx", 2), _rs(dx),
-                         _dev(dw, "dw", 1), _dev(db, "db", 1),
-                         DTYPE_CODE[gd.dtype] if gd is not None else NORM_F32,
-                         _dev(workspace, "workspace"), ws_bytes, M, N, float(offset), float(eps),
-                         DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream, x))
-    _check("norm_ln_bwd", rc)
+    wdt = _weight(w, N)
+    _mat(dy, "dy", M, N, dt)
+    _mat(dx, "dx", M, N, dt)
+    _vec(mean, "mean", M, _F32, at_least=True, required=False)
+    _vec(rstd, "rstd", M, _F32, at_least=True, required=False)
+    _vec(dw, "dw", N, (torch.float32, wdt), required=False)
+    _vec(db, "db", N, (torch.float32, wdt), required=False)
+    dwt = _grad_dtype(wdt, ("dw", dw), ("db", db))
+    dev = _device(x, ("dy", dy), ("w", w), ("mean", mean), ("rstd", rstd), ("dx", dx), ("dw", dw), ("db", db),
+                  ("workspace", workspace))
+    wsp, wsb = _ws(workspace)
+    _on(dev, lambda: _check("norm_ln_bwd", lib.norm_ln_bwd(
+        _ptr(dy), _rs(dy), _ptr(x), _rs(x), _ptr(w), _ptr(mean), _ptr(rstd), _ptr(dx), _rs(dx), _ptr(dw),
+        _ptr(db), dwt, wsp, wsb, M, N, float(offset), float(eps), DTYPE_CODE[dt], DTYPE_CODE[wdt],
+        _stream(stream, x))))
 
 
 def norm_fused_add_rms_fwd(x, residual, w, y, h_out, rstd=None, offset=0.0, eps=1e-6, stream=None):
     """h_out = x + residual (rounded), y = RMSNorm(h) with scale (w + offset)."""
+    dt = _act_dtype(x)
     M, N = x.shape
-    rc = lib.norm_fused_add_rms_fwd(_dev(x, "x", 2), _rs(x), _dev(residual, "residual", 2), _rs(residual),
-                                    _dev(w, "w", 1), _dev(y, "y", 2), _rs(y), _dev(h_out, "h_out", 2),
-                                    _rs(h_out), _dev(rstd, "rstd", 1), M, N, float(offset), float(eps),
-                                    DTYPE_CODE[x.dtype], DTYPE_CODE[w.dtype], _stream(stream, x))
-    _check("norm_fused_add_rms_fwd", rc)
+    wdt = _weight(w, N)
+    _mat(residual, "residual", M, N, dt)
+    _mat(y, "y", M, N, dt)
+    _mat(h_out, "h_out", M, N, dt)
+    _vec(rstd, "rstd", M, _F32, at_least=True, required=False)
+    dev = _device(x, ("residual", residual), ("w", w), ("y", y), ("h_out", h_out), ("rstd", rstd))
+    _on(dev, lambda: _check("norm_fused_add_rms_fwd", lib.norm_fused_add_rms_fwd(
+        _ptr(x), _rs(x), _ptr(residual), _rs(residual), _ptr(w), _ptr(y), _rs(y), _ptr(h_out), _rs(h_out),
+        _ptr(rstd), M, N, float(offset), float(eps), DTYPE_CODE[dt], DTYPE_CODE[wdt], _stream(stream, x))))
 
 
 def norm_fused_add_rms_bwd(dy, dh_out, h, w, rstd, dx, dw=None, workspace=None, offset=0.0, eps=1e-6,
                            stream=None):
     """dx (= d residual) and dw unless None, of FusedAddRMSNorm at saved h."""
+    dt = _act_dtype(h, "h")
     M, N = h.shape
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib.norm_fused_add_rms_bwd(_dev(dy, "dy", 2), _rs(dy), _dev(dh_out, "dh_out", 2), _rs(dh_out),
-                                    _dev(h, "h", 2), _rs(h), _dev(w, "w", 1), _dev(rstd, "rstd", 1),
-                                    _dev(dx, "dx", 2), _rs(dx), _dev(dw, "dw", 1),
-                                    DTYPE_CODE[dw.dtype] if dw is not None else NORM_F32,
-                                    _dev(workspace, "workspace"), ws_bytes, M, N, float(offset), float(eps),
-                                    DTYPE_CODE[h.dtype], DTYPE_CODE[w.dtype], _stream(stream, h))
-    _check("norm_fused_add_rms_bwd", rc)
+    wdt = _weight(w, N)
+    _mat(dy, "dy", M, N, dt)
+    _mat(dh_out, "dh_out", M, N, dt, required=False)
+    _mat(dx, "dx", M, N, dt)
+    _vec(rstd, "rstd", M, _F32, at_least=True, required=False)
+    _vec(dw, "dw", N, (torch.float32, wdt), required=False)
+    dwt = _grad_dtype(wdt, ("dw", dw))
+    dev = _device(h, ("dy", dy), ("dh_out", dh_out), ("w", w), ("rstd", rstd), ("dx", dx), ("dw", dw),
+                  ("workspace", workspace))
+    wsp, wsb = _ws(workspace)
+    _on(dev, lambda: _check("norm_fused_add_rms_bwd", lib.norm_fused_add_rms_bwd(
+        _ptr(dy), _rs(dy), _ptr(dh_out), _rs(dh_out), _ptr(h), _rs(h), _ptr(w), _ptr(rstd), _ptr(dx), _rs(dx),
+        _ptr(dw), dwt, wsp, wsb, M, N, float(offset), float(eps), DTYPE_CODE[dt], DTYPE_CODE[wdt],
+        _stream(stream, h))))

@@ -26,3 +26,25 @@ def built_package():
     load_build_module().build()
     import row_normalization_rmsnorm_gb300 as pkg
     return pkg
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Summary of the parity checks run in this session: for every output
+    checked against the oracle, how many elements passed only through the
+    cancellation floor (the n_floor_only count of tests/tolerance.py)."""
+    try:
+        from tolerance import REPORTS
+    except ImportError:
+        return
+    reps = [r for r in REPORTS if r.get("label")]
+    if not reps:
+        return
+    tr = terminalreporter
+    n = sum(r["n"] for r in reps)
+    nf = sum(r["n_floor_only"] for r in reps)
+    tr.section("parity checks: elements passing only through the cancellation floor")
+    tr.write_line(f"{len(reps)} checks, {n} elements, {nf} floor-only ({100.0 * nf / max(n, 1):.4f} %)")
+    worst = sorted(reps, key=lambda r: -r["n_floor_only"] / max(r["n"], 1))[:12]
+    for r in worst:
+        tr.write_line(f"  {r['label'][:60]:60s} n={r['n']:>10d} floor_only={r['n_floor_only']:>7d} "
+                      f"({100.0 * r['n_floor_only'] / max(r['n'], 1):.3f} %) rel_l2={r['rel_l2']:.2e}")

@@ -76,3 +76,30 @@ def test_reference_arm_prints_one_contract_line():
     assert j["steps"] == 2 and j["warmup"] == 1 and j["value"] > 0
     assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["value"] == j["value"]
     assert j["e2e"] == {"value": j["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_cpu_baseline_runs_on_every_core_and_keeps_the_single_thread_figure():
+    host = bench.host_inputs(64, 512, seed=0)
+    cb = bench.cpu_baseline(host, target_s=0.3)
+    assert cb["kind"] == "oracle" and cb["unit"] == "GB/s"
+    assert cb["cores"] == bench.host_cores() >= 1
+    assert cb["value"] > 0 and cb["single_thread_value"] > 0
+    assert f"on {cb['cores']} threads" in cb["sample"]
+
+
+def test_parallel_oracle_blocks_partition_the_sample():
+    # the row blocks cover the sample exactly once, in order, and the block
+    # partial sums of dW add up (in block order) to the one-block result
+    import numpy as np
+    host = bench.host_inputs(40, 256, seed=1)
+    one, w, lb = bench.oracle_blocks(host, 40, 1)
+    many, _, _ = bench.oracle_blocks(host, 40, 6)
+    assert sum(b["rx"].shape[0] for b in many) == 40
+    np.testing.assert_array_equal(np.concatenate([b["lx"] for b in many]), one[0]["lx"])
+    ref = bench.oracle_block(one[0], w, lb)
+    parts = [bench.oracle_block(b, w, lb) for b in many]
+    for k in range(4):
+        tot = parts[0][k].copy()
+        for p in parts[1:]:
+            tot += p[k]
+        np.testing.assert_allclose(tot, ref[k], rtol=1e-12, atol=1e-12)

@@ -3,16 +3,19 @@ workspace version (norm_rms_bwd), through the C ABI.
 
 norm_rms_bwd_noalloc serves callers that cannot allocate device memory: it
 keeps the dW partial sums in the library's fixed scratch array instead of a
-caller-provided workspace.  Two calls in a row (different inputs) must match
-the workspace version within the parity tolerance; a problem too large for
-the scratch is refused before anything runs.  This file is collected last so
+caller-provided workspace.  It runs the same kernels with the same launch
+shape as the workspace version, so two calls in a row (different inputs)
+must give bit-identical dx and dW; the second is also checked against the
+FP64 oracle.  A problem too large for the scratch is refused before anything
+runs.  This file is collected last so
 that a stop at its first failure has already run every other test.
 """
 import pytest
 import torch
 
 import synthetic_inputs as si
-from gpu_util import workspace
+import oracle
+from gpu_util import bits_equal, dw_scale, f64, unit_xhat, workspace
 from tolerance import check, check_dw, dtype_name
 
 pytestmark = pytest.mark.gpu
@@ -45,10 +48,14 @@ def test_noalloc_matches_workspace_version_twice(g):
     assert g.lib.norm_noalloc_scratch_bytes() >= g.norm_bwd_workspace_bytes(8192, 8192, True)
     for case, dw_dtype, offset in cases:
         dx_ws, dw_ws, dx_na, dw_na = run_both(g, case, dw_dtype, offset)
-        tn = dtype_name(dx_ws)
-        check(dx_na, dx_ws.double().cpu().numpy(), tn, label="noalloc dx")
-        ref = dw_ws.double().cpu().numpy()
-        check_dw(dw_na, ref, dtype_name(dw_na), abs(ref), label="noalloc dw")
+        assert bits_equal(dx_na, dx_ws), "noalloc dx differs from the workspace call"
+        assert bits_equal(dw_na, dw_ws), "noalloc dW differs from the workspace call"
+    # the last call against the oracle (saved-rstd path, as the GPU used its forward's rstd)
+    x, dy, w = (f64(case[k]) for k in ("x", "dy", "w"))
+    rstd = oracle.rms_fwd(x, w, offset, 1e-6)[1]
+    dxr, dwr, sc = oracle.rms_bwd(x, dy, w, offset, 1e-6, with_scale=True, rstd=rstd)
+    check(dx_na, dxr, dtype_name(dx_na), scale=sc, label="noalloc dx vs oracle")
+    check_dw(dw_na, dwr, dtype_name(dw_na), dw_scale(dy, unit_xhat(x, False, 1e-6)), label="noalloc dw vs oracle")
 
 
 def test_noalloc_refuses_a_problem_larger_than_its_scratch(g):

@@ -26,6 +26,11 @@ FLOOR = {"float32": 2.0 ** -17, "float16": 2.0 ** -16, "bfloat16": 2.0 ** -16}
 REL_F32 = 1e-5
 DW_REL_L2 = 1e-4
 
+# Every check() report of this test session, printed as a summary at the end
+# of the run (tests/conftest.py): how many elements of each output passed
+# only through the floor clause.
+REPORTS: list = []
+
 _NAMES = {torch.float32: "float32", torch.float16: "float16", torch.bfloat16: "bfloat16"}
 
 
@@ -86,6 +91,7 @@ def check(gpu, ref, name_out: str, scale=None, label: str = "", max_floor_frac=1
     rep = Report(label=label, n=int(r.size), n_floor_only=n_floor,
                  max_abs=float(err.max()) if err.size else 0.0,
                  rel_l2=float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-300)))
+    REPORTS.append(rep)
     if not ok.all():
         bad = np.flatnonzero(~ok)
         worst = bad[np.argsort(-err[bad])[:8]]
