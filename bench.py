@@ -105,10 +105,15 @@ def host_inputs(M, N, seed=0):
 
 
 class Workload:
-    """Device tensors of one step; `run(op)` issues one operation."""
+    """Device tensors of one step; `run(op)` issues one operation.
 
-    def __init__(self, g, host, M, N, dev="cuda"):
-        self.g, self.M, self.N = g, M, N
+    With world > 1 the rows are this rank's shard of one M-sharded problem:
+    a trainable backward then reduces this rank's dW / dB in FP32 and sums
+    them over the ranks in rank order (dist.sharded_backward), inside the
+    call."""
+
+    def __init__(self, g, host, M, N, dev="cuda", world=1):
+        self.g, self.M, self.N, self.world = g, M, N, world
         bf = torch.bfloat16
         e = lambda: torch.empty(M, N, dtype=bf, device=dev)  # noqa: E731
         f32 = lambda n: torch.empty(n, dtype=torch.float32, device=dev)  # noqa: E731
@@ -126,10 +131,24 @@ class Workload:
         self.t["fadd.h"] = e()
         nb = max(g.norm_bwd_workspace_bytes(M, N, True, True), 16)
         self.ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        if world > 1:
+            from row_normalization_rmsnorm_gb300 import dist as gdist
+            self.gdist = gdist
+            self.partials = {k: (f32(N), f32(N)) for k in ("rms", "ln", "fadd")}
 
     def run(self, op, trainable=True, stream=None):
         g, t = self.g, self.t
         ws = self.ws if trainable else None
+        if self.world > 1 and trainable and op.endswith("_bwd"):
+            # one M-sharded problem: dW / dB combined over the ranks
+            k = op[:-4]
+            stats = {"rms": t["rms.rstd"], "ln": (t["ln.mean"], t["ln.rstd"]), "fadd": t["fadd.rstd"]}[k]
+            x = t["fadd.h"] if k == "fadd" else t[f"{k}.x"]
+            self.gdist.sharded_backward(k, t[f"{k}.dy"], x, t[f"{k}.w"], stats, t[f"{k}.dx"], t[f"{k}.dw"],
+                                        t["ln.db"] if k == "ln" else None,
+                                        t["fadd.dh_out"] if k == "fadd" else None, 0.0, 1e-6, ws,
+                                        self.partials[k])
+            return
         if op == "rms_fwd":
             g.norm_rms_fwd(t["rms.x"], t["rms.w"], t["rms.y"], t["rms.rstd"], 0.0, 1e-6, stream)
         elif op == "ln_fwd":
@@ -380,11 +399,25 @@ def main():
     ap.add_argument("--grid", action="store_true",
                     help="run every operation of the shape grid twice, untimed, and print the call order "
                          "(for an ncu kernel-duration capture)")
+    ap.add_argument("--traffic", action="store_true",
+                    help="run each operation once after an L2 flush and before a read-only L2 scrub, untimed, "
+                         "for an ncu DRAM-bytes capture that includes the operation's deferred write-backs")
+    ap.add_argument("--traffic-from", metavar="CSV",
+                    help="summarise an ncu CSV of a --traffic run into profiles/ncu_traffic_<M>x<N>.json")
+    ap.add_argument("--grid-from", nargs=2, metavar=("CSV", "ORDER_LOG"),
+                    help="print a markdown table of an ncu kernel-duration CSV of a --grid run, given the "
+                         "grid run's own output (its call order)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
     if args.grid:
         return run_grid()
+    if args.traffic:
+        return run_traffic(args.M, args.N)
+    if args.traffic_from:
+        return summarise_traffic(args.traffic_from, args.M, args.N)
+    if args.grid_from:
+        return summarise_grid(*args.grid_from)
 
     import row_normalization_rmsnorm_gb300 as g
     from row_normalization_rmsnorm_gb300 import dist as gdist
@@ -398,7 +431,7 @@ def main():
     ops = [o for o in args.ops.split(",") if o]
     assert all(o in OPS for o in ops), ops
     host = host_inputs(M, N, seed=rank)
-    wl = Workload(g, host, M, N)
+    wl = Workload(g, host, M, N, world=ws)
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
@@ -449,6 +482,9 @@ def main():
         b = op_bytes(op, M, N)
         per_op[op] = {"us": us, "GBps": b / us / 1e3, "frac": b / us / 1e3 / peak, "bytes": b}
     for op in ([] if args.no_extras else [o for o in ("rms_bwd", "ln_bwd", "fadd_bwd") if o in ops]):
+        # the first call of the frozen instantiation loads its code: untimed
+        wl.run(op, False, stream)
+        torch.cuda.synchronize()
         ts = []
         for _ in range(max(5, min(50, args.steps // 2))):
             flush_l2()
@@ -488,7 +524,11 @@ def main():
                        "l2": "flushed before every step (zero-fill of 2x L2, then a read of another 2x L2 "
                              "so the flush's dirty lines are written back before timing); every tensor > L2",
                        "timing": "CUDA events on the launching stream; flush excluded",
-                       "wall_s_timed_region": wall, "parallelism": f"replicas x{ws}"},
+                       "wall_s_timed_region": wall,
+                       "parallelism": ("1 GPU" if ws == 1 else
+                                       f"M-sharded x{ws}: each rank normalises {M} rows of one {M * ws}x{N} "
+                                       "problem; the backward's dW/dB are summed over ranks in rank order "
+                                       "(NCCL all_gather) inside the step")},
             "roofline": roofline,
             "per_op": per_op,
             "shapes": shapes,
@@ -643,6 +683,131 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
+TRAFFIC_ORDER = OPS   # the operations of a --traffic run, in launch order
+
+
+def run_traffic(M, N):
+    """One round of warm-up, then for each operation of the step: an L2 flush
+    (a write, then a read, of 2x L2), the operation (trainable), and a
+    read-only scrub of 2x L2.  The scrub only reads, so the DRAM bytes it
+    writes are the operation's dirty lines evicted from L2: an ncu capture of
+    dram__bytes_read/write over every launch, with ncu's own cache flushing
+    off (--cache-control none), gives each operation's whole DRAM traffic,
+    its deferred write-backs included (--traffic-from)."""
+    import row_normalization_rmsnorm_gb300 as g
+    torch.cuda.set_device(0)
+    st = torch.cuda.current_stream()
+    wl = Workload(g, host_inputs(M, N, 0), M, N)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
+    scrub = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device="cuda").fill_(1.0)
+    for op in TRAFFIC_ORDER:   # warm-up: code loaded, launch shapes cached
+        wl.run(op, True, st)
+    torch.cuda.synchronize()
+    for op in TRAFFIC_ORDER:
+        flush.zero_()
+        scrub.sum()
+        wl.run(op, True, st)
+        scrub.sum()
+    torch.cuda.synchronize()
+    print(json.dumps({"traffic_order": TRAFFIC_ORDER, "M": M, "N": N}), flush=True)
+    return 0
+
+
+def summarise_traffic(csv_path, M, N):
+    """Per-call DRAM bytes of every operation from an ncu CSV of a --traffic
+    run (metrics dram__bytes_read.sum, dram__bytes_write.sum per launch):
+    the last len(OPS) groups of [flush write, flush read, op kernels, scrub]
+    are attributed in launch order; an operation's traffic is its kernels'
+    reads and writes plus the writes of the scrub after it."""
+    import csv
+    rows = {}
+    with open(csv_path, newline="") as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    for r in csv.DictReader(lines):
+        key = (int(r["ID"]), r["Kernel Name"])
+        v = float(r["Metric Value"].replace(",", ""))
+        unit = r.get("Metric Unit", "byte")
+        scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1024, "MB": 1 << 20, "GB": 1 << 30}.get(unit, 1)
+        rows.setdefault(key, {})[r["Metric Name"]] = v * scale
+    launches = [(k[1], m) for k, m in sorted(rows.items())]
+    ours = lambda name: any(t in name for t in ("staged_kernel", "loop_kernel", "colreduce"))  # noqa: E731
+    # walk backwards: each operation is a run of our kernels followed by one scrub (a torch reduction)
+    out, i = {}, len(launches) - 1
+    for op in reversed(TRAFFIC_ORDER):
+        scrub = launches[i]
+        assert not ours(scrub[0]), scrub[0]
+        j = i - 1
+        kernels = []
+        while j >= 0 and ours(launches[j][0]):
+            kernels.append(launches[j])
+            j -= 1
+        kernels.reverse()
+        rd = sum(m.get("dram__bytes_read.sum", 0.0) for _, m in kernels)
+        wr = sum(m.get("dram__bytes_write.sum", 0.0) for _, m in kernels)
+        wb = scrub[1].get("dram__bytes_write.sum", 0.0)
+        out[op] = {"kernels": [n for n, _ in kernels], "dram_read": rd, "dram_write": wr,
+                   "deferred_write_back": wb, "per_call": rd + wr + wb,
+                   "algorithmic": op_bytes(op, M, N), "ratio": (rd + wr + wb) / op_bytes(op, M, N)}
+        i = j - 2   # skip the flush's write and read kernels
+    res = {"workload": f"bf16 {M}x{N}, one call per operation, trainable", "source_hash": kernel_source_hash(),
+           "command": f"ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
+                      f"--cache-control none --clock-control none --csv --log-file traffic.csv "
+                      f"python bench.py --traffic --M {M} --N {N}",
+           "note": "per_call = the operation's kernels' DRAM reads and writes plus the DRAM writes of the "
+                   "read-only L2 scrub that follows it (its dirty lines written back late)",
+           "traffic": out}
+    path = os.path.join(ROOT, "profiles", f"ncu_traffic_{M}x{N}.json")
+    with open(path, "w") as f:
+        json.dump(res, f, indent=1)
+    print(json.dumps({k: round(v["ratio"], 4) for k, v in out.items()}))
+    return 0
+
+
+def summarise_grid(csv_path, order_log):
+    """Markdown table of a --grid ncu capture (gpu__time_duration.sum of our
+    kernels, in launch order): for each (shape, operation) the second of its
+    two calls, row kernel plus column reduce, with GB/s of algorithmic bytes
+    and the fraction of the measured HBM peak."""
+    import csv
+    order = None
+    with open(order_log) as f:
+        for ln in f:
+            if ln.startswith("{") and "grid_order" in ln:
+                order = json.loads(ln)["grid_order"]
+    with open(csv_path, newline="") as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    launches = []
+    for r in csv.DictReader(lines):
+        if r["Metric Name"] == "gpu__time_duration.sum":
+            unit = r.get("Metric Unit", "ns")
+            v = float(r["Metric Value"].replace(",", "")) * {"ns": 1e-3, "us": 1.0, "usecond": 1.0,
+                                                             "nsecond": 1e-3, "ms": 1e3, "msecond": 1e3}.get(unit, 1e-3)
+            launches.append((int(r["ID"]), r["Kernel Name"], v))
+    launches.sort()
+    peak, kind = measured_peak()
+    rows, i = [], 0
+    for M, N, op, tr, rep in order:
+        n = 2 if (op.endswith("_bwd") and tr) else 1
+        ks = launches[i:i + n]
+        i += n
+        if rep != 1:
+            continue
+        row_us = ks[0][2]
+        cr_us = ks[1][2] if n == 2 else 0.0
+        b = op_bytes(op, M, N, trainable=tr)
+        gbs = b / (row_us + cr_us) / 1e3
+        name = ks[0][1].replace("gb300norm::", "").replace("__nv_bfloat16", "bf16").split("(")[0]
+        rows.append(f"| {M}×{N} | {op}{'' if tr or not op.endswith('_bwd') else ' frozen'} | {row_us:.1f} | "
+                    f"{cr_us:.1f} | {gbs:.0f} | {100 * gbs / peak:.0f} % | `{name}` |")
+    assert i == len(launches), (i, len(launches))
+    print(f"| shape | op | row kernel µs | + column reduce µs | GB/s (row + reduce) | % of {kind} {peak:.0f} GB/s "
+          f"| kernel |")
+    print("|---|---|---|---|---|---|---|")
+    print("\n".join(rows))
+    return 0
+
+
 def load_profile_traffic(op, M, N):
     """DRAM bytes (read + write) per call of the operation's kernels, from the
     committed ncu capture of this exact workload -- or None when there is
@@ -706,8 +871,44 @@ def run_e2e(wl, stream, steps, M, N, ops):
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
     step_bytes = sum(op_bytes(op, M, N) for op in ops)
+    roof = copy_roof(wl, host_in, host_out, stream, side)
+    roof["value_at_roof"] = step_bytes / (roof["both_ms"] * 1e-3) / 1e9
+    roof["frac"] = roof["both_ms"] / ms
     return {"value": step_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "copy_roof": roof}
+
+
+def copy_roof(wl, host_in, host_out, stream, side, reps=3):
+    """The e2e step's own roof, measured in the same run: the step's uploads
+    alone, its downloads alone, and both at once on two streams (the two
+    directions of the host link), each the best of `reps` event-timed
+    rounds.  `both_ms` is the least time the e2e step could take if its
+    kernels cost nothing."""
+    def timed(up, down):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            side.wait_event(a)
+            if up:
+                for k, v in host_in.items():
+                    wl.t[k].copy_(v, non_blocking=True)
+            if down:
+                with torch.cuda.stream(side):
+                    for k, v in host_out.items():
+                        v.copy_(wl.t[k], non_blocking=True)
+            stream.wait_stream(side)
+            b.record(stream)
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b))
+        return best
+    up_ms, down_ms, both_ms = timed(True, False), timed(False, True), timed(True, True)
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    return {"h2d_GBps": h2d / (up_ms * 1e-3) / 1e9, "d2h_GBps": d2h / (down_ms * 1e-3) / 1e9,
+            "both_ms": both_ms, "both_GBps": (h2d + d2h) / (both_ms * 1e-3) / 1e9,
+            "how": "pinned host buffers of the step, cudaMemcpyAsync per tensor, best of 3 (CUDA events)"}
 
 
 if __name__ == "__main__":

@@ -238,9 +238,12 @@ GB300NORM_API int norm_rms_bwd_noalloc(const void *dy, int64_t dy_stride,
  * Device-side status word shared by all kernels of this library on the
  * current device: 0 when no kernel has reported a problem.  A kernel whose
  * bounded wait for an asynchronous row copy runs out sets it (non-zero) and
- * returns early instead of hanging.  This call synchronises the device; with
- * reset != 0 the word is cleared afterwards.  Returns NORM_OK or
- * NORM_ERR_CUDA; *value receives the word.
+ * returns early instead of hanging.  While the word is non-zero the outputs
+ * of the calls issued since it was last cleared are undefined: rows after
+ * the failed wait are not written, and dW / dB are not valid (the CTA that
+ * gave up writes no partial sums, but the column reduction still runs).
+ * This call synchronises the device; with reset != 0 the word is cleared
+ * afterwards.  Returns NORM_OK or NORM_ERR_CUDA; *value receives the word.
  */
 GB300NORM_API int norm_device_status(int reset, int *value);
 
@@ -264,8 +267,10 @@ GB300NORM_API int norm_debug_set_path(int mode);
  * Test hook for launch-shape sweeps: key 1 = 16-byte chunks per thread of the
  * aligned-row kernels (1, 2, 4 or 8), key 2 = maximum CTAs per SM, key 3 =
  * maximum pipeline stages, key 4 = cap on row bytes in flight per SM in
- * units of 16 KB (64 = no cap in practice); value 0 restores the automatic
- * choice (values 0..64).  Affects
+ * units of 16 KB (64 = no cap in practice), key 5 = CTAs per row (1, 2, 4
+ * or 8: a thread-block cluster splitting each row into equal column
+ * slices; a split that does not divide the row's 16-byte chunks is not
+ * used); value 0 restores the automatic choice (values 0..64).  Affects
  * speed only, never results of the same kernel family except through the
  * reduction tree shape.  Returns NORM_OK or NORM_ERR_ARG.
  */

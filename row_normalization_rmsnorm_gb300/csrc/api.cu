@@ -25,7 +25,7 @@ int cuda_fail(cudaError_t e) {
 namespace {
 
 std::atomic<int> g_force_path{0};
-std::atomic<int> g_tune[5] = {{0}, {0}, {0}, {0}, {0}};
+std::atomic<int> g_tune[6] = {{0}, {0}, {0}, {0}, {0}, {0}};
 
 int elem_size(int dt) {
   switch (dt) {
@@ -78,6 +78,7 @@ int get_device(DevInfo* out, int** status) {
   out->tune_max_ctas = g_tune[2].load();
   out->tune_max_stages = g_tune[3].load();
   out->tune_inflight_16k = g_tune[4].load();
+  out->tune_cluster = g_tune[5].load();
   if (status) *status = g_dev.status[dev];
   return NORM_OK;
 }
@@ -249,7 +250,8 @@ int norm_debug_set_path(int mode) {
 }
 
 int norm_debug_tune(int key, int value) {
-  if (key < 1 || key > 4 || value < 0 || value > 64) return NORM_ERR_ARG;
+  if (key < 1 || key > 5 || value < 0 || value > 64) return NORM_ERR_ARG;
+  if (key == 5 && value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return NORM_ERR_ARG;
   g_tune[key].store(value);
   return NORM_OK;
 }

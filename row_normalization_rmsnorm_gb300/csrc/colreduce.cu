@@ -58,7 +58,8 @@ __global__ void __launch_bounds__(256) colreduce_kernel(const float* __restrict_
 
 // The form for many partial rows (G >= kCrClusterRows, N % 4 == 0: every
 // partial row then starts on a 16-byte boundary, as the workspace is 16-byte
-// aligned and the dB partials start G * N floats after the dW ones).  A
+// aligned and the dB partials start partial_rows(M, N, SMs) * N floats after
+// the dW ones, see run_bwd in api.cu).  A
 // thread-block cluster of kCrCluster CTAs owns 128 adjacent columns (lane l:
 // columns 4l..4l+3, 16-byte loads) and splits the G partial rows among its
 // kCrCluster x 8 warps: warp w of CTA r takes rows (8r + w) + 8 kCrCluster i,

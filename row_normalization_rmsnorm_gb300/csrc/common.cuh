@@ -174,23 +174,60 @@ __device__ __forceinline__ void warp_sum(float (&v)[NV]) {
 // warp, whatever a given call uses, so consecutive calls never share slots.
 constexpr int kMaxReduceValues = 2;
 
+// Two values reduced together: one packed add per butterfly step.
+__device__ __forceinline__ void warp_sum2(float2& v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float2 t = make_float2(__shfl_xor_sync(0xffffffffu, v.x, o), __shfl_xor_sync(0xffffffffu, v.y, o));
+    v = fadd2(v, t);
+  }
+}
+
+// A CTA-wide sum in two halves around one barrier: reduce_warps sums each
+// warp's values and has lane 0 store them in bank `bank` of `red`;
+// reduce_finish (after a __syncthreads) sums the warps' values.  Every warp
+// reduces the same warp partials with the same butterfly, so every thread of
+// the CTA ends with the same bits.  Two values go through packed adds.
+template <int NV>
+__device__ __forceinline__ void reduce_warps(float (&v)[NV], float* red, int bank) {
+  static_assert(NV <= kMaxReduceValues, "bank size");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* r = red + bank * 32 * kMaxReduceValues;
+  if constexpr (NV == 2) {
+    float2 s = make_float2(v[0], v[1]);
+    warp_sum2(s);
+    if (lane == 0) reinterpret_cast<float2*>(r)[warp] = s;
+  } else {
+    warp_sum<NV>(v);
+    if (lane == 0) {
+#pragma unroll
+      for (int i = 0; i < NV; ++i) r[warp * NV + i] = v[i];
+    }
+  }
+}
+
+template <int NV>
+__device__ __forceinline__ void reduce_finish(float (&v)[NV], const float* red, int bank) {
+  const int lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
+  const float* r = red + bank * 32 * kMaxReduceValues;
+  if constexpr (NV == 2) {
+    float2 s = (lane < nw) ? reinterpret_cast<const float2*>(r)[lane] : make_float2(0.f, 0.f);
+    warp_sum2(s);
+    v[0] = s.x;
+    v[1] = s.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = (lane < nw) ? r[lane * NV + i] : 0.f;
+    warp_sum<NV>(v);
+  }
+}
+
 template <int NV>
 __device__ __forceinline__ void block_sum(float (&v)[NV], float* red, int& bank) {
-  static_assert(NV <= kMaxReduceValues, "bank size");
-  warp_sum<NV>(v);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nw = blockDim.x >> 5;
-  float* r = red + bank * 32 * kMaxReduceValues;
-  if (lane == 0) {
-#pragma unroll
-    for (int i = 0; i < NV; ++i) r[warp * NV + i] = v[i];
-  }
+  reduce_warps<NV>(v, red, bank);
   __syncthreads();
-  // Every warp reduces the same warp partials with the same butterfly, so
-  // every thread of the CTA ends with the same bits.
-#pragma unroll
-  for (int i = 0; i < NV; ++i) v[i] = (lane < nw) ? r[lane * NV + i] : 0.f;
-  warp_sum<NV>(v);
+  reduce_finish<NV>(v, red, bank);
   bank ^= 1;
 }
 
@@ -200,11 +237,23 @@ __device__ __forceinline__ float tree_sum(const float (&a)[VEC]) {
   if constexpr (VEC == 4) return fadd(fadd(a[0], a[1]), fadd(a[2], a[3]));
   else return fadd(fadd(fadd(a[0], a[1]), fadd(a[2], a[3])), fadd(fadd(a[4], a[5]), fadd(a[6], a[7])));
 }
-// The same sum over accumulators held as pairs (lanes 2h, 2h+1 in a[h]).
+// The same sum over accumulators held as pairs (lanes 2h, 2h+1 in a[h]):
+// the pairs are added lane-wise first (packed), then the two lanes.
+template <int H>
+__device__ __forceinline__ float2 pair_tree(const float2 (&a)[H]) {
+  if constexpr (H == 2) return fadd2(a[0], a[1]);
+  else return fadd2(fadd2(a[0], a[1]), fadd2(a[2], a[3]));
+}
 template <int H>
 __device__ __forceinline__ float tree_sum(const float2 (&a)[H]) {
-  if constexpr (H == 2) return fadd(fadd(a[0].x, a[0].y), fadd(a[1].x, a[1].y));
-  else return fadd(fadd(fadd(a[0].x, a[0].y), fadd(a[1].x, a[1].y)), fadd(fadd(a[2].x, a[2].y), fadd(a[3].x, a[3].y)));
+  const float2 t = pair_tree<H>(a);
+  return fadd(t.x, t.y);
+}
+// Two such sums at once: (sum of a, sum of b).
+template <int H>
+__device__ __forceinline__ float2 tree_sum_2(const float2 (&a)[H], const float2 (&b)[H]) {
+  const float2 s = pair_tree<H>(a), t = pair_tree<H>(b);
+  return fadd2(make_float2(s.x, t.x), make_float2(s.y, t.y));
 }
 
 // 1/sqrt(m + eps).
@@ -262,15 +311,47 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // otherwise never finish.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 
-// Wait until the phase with the given parity of `bar` has completed.
-// Returns false (and leaves the barrier untouched) if kWaitLimitNs passes.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Wait until the phase with the given parity of `bar` has completed, or
+// until the global timer passes `deadline` (ns); false in the second case
+// (the barrier is left untouched).
+__device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, uint64_t deadline) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() > deadline) return false;
+  }
+}
+
+// The same with a limit of kWaitLimitNs from now.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_until(bar, parity, global_timer_ns() + kWaitLimitNs);
+}
+
+// try_wait with acquire semantics at cluster scope: for a phase completed by
+// other CTAs' stores into this CTA's shared memory (released at cluster
+// scope), so that their data is visible once the phase is seen complete.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "n"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded (kWaitLimitNs) wait with cluster-scope acquire.
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t deadline = global_timer_ns() + kWaitLimitNs;
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (global_timer_ns() > deadline) return false;
   }
 }
 
@@ -307,6 +388,47 @@ __device__ __forceinline__ void st_global_cs16(void* p, uint4 v) {
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Thread-block clusters (sm_90+ instructions, used on sm_103a)
+// ---------------------------------------------------------------------------
+// CTAs in this CTA's cluster (1 when the kernel was not launched as a
+// cluster), and this CTA's rank among them.
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster arrives, then waits for all the
+// others; shared-memory writes before it are visible to the cluster after.
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The address, in CTA `rank` of the cluster, of the variable at shared
+// address `addr` of this CTA.
+__device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Asynchronous store of one or two floats into another CTA's shared memory,
+// completing their bytes on that CTA's mbarrier.
+__device__ __forceinline__ void st_async_f32(uint32_t remote, float a, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];"
+               ::"r"(remote), "f"(a), "r"(remote_bar) : "memory");
+}
+__device__ __forceinline__ void st_async_f32x2(uint32_t remote, float a, float b, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+               ::"r"(remote), "f"(a), "f"(b), "r"(remote_bar) : "memory");
 }
 
 // Status bits written to RowParams::status.

@@ -61,7 +61,20 @@ __host__ __device__ constexpr size_t staged_col_bytes(int N, bool wreg) {
   return wreg ? 0 : ((size_t)N * 4 * (OP == LN_FWD ? 2 : 1) + 127) / 128 * 128;
 }
 
-template <int OP, class T, class TW, int NPT, bool DW, bool DB>
+// EXACT: the CTA's threads own exactly its nchunks chunks (threads x NPT ==
+// nchunks), so no per-chunk bounds test is compiled into the row loop.
+//
+// CL: launched as thread-block clusters of C CTAs (C = 2, 4 or 8), the C
+// CTAs of a cluster split every row of the cluster into C equal column
+// slices: each streams, reduces and writes only its slice, and the CTAs
+// exchange their row sums through distributed shared memory (each stores
+// its sums into every peer with st.async, completing on the peer's
+// mbarrier) and add them in rank order, so all CTAs of the cluster hold the
+// same bits.  This serves rows that one CTA cannot take without spilling
+// registers (more than 4096 chunks, or the per-column state of a wide
+// backward).  The dW / dB partial row of a cluster is written slice by
+// slice by its CTAs.  Without CL the cluster code is compiled out.
+template <int OP, class T, class TW, int NPT, bool DW, bool DB, bool EXACT, bool CL>
 __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const int S) {
   constexpr int VEC = 16 / (int)sizeof(T);
   constexpr int H = VEC / 2;   // element pairs per chunk
@@ -83,33 +96,45 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
   constexpr int NR = (OP == LN_BWD) ? 2 : 1;     // values reduced per backward row
   using P = Pack16<T>;
   const int N = p.N;
-  const int nchunks = N / VEC;
+  // cluster: C CTAs, this one's rank, and its slice of chunks (the launcher
+  // makes the slices equal): chunk c of the slice is chunk col0 + c of a row
+  const int ncl = CL ? (int)cluster_nctarank() : 1;
+  const int crank = CL ? (int)cluster_ctarank() : 0;
+  const int nchunks = N / VEC / ncl;
+  const int col0 = crank * nchunks;
+  const int NL = nchunks * VEC;   // columns of the slice
   const int tid = threadIdx.x, nt = blockDim.x;
-  const uint32_t row_bytes = (uint32_t)N * (uint32_t)sizeof(T);
+  const uint32_t row_bytes = (uint32_t)nchunks * 16u;
   const int nin = (OP == FADD_BWD && p.in2 == nullptr) ? 2 : OpInfo<OP>::NIN;
   const uint32_t stage_bytes = (uint32_t)nin * row_bytes;
 
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   float* red = reinterpret_cast<float*>(smem + 256);
-  float* wsm = reinterpret_cast<float*>(smem + kStagedHeader);   // W' [N] (+ bias [N]) when !WREG
-  unsigned char* stages = smem + kStagedHeader + staged_col_bytes<OP>(N, WREG);
+  float* wsm = reinterpret_cast<float*>(smem + kStagedHeader);   // W' [NL] (+ bias [NL]) when !WREG
+  unsigned char* stages = smem + kStagedHeader + staged_col_bytes<OP>(NL, WREG);
   // abort_flag[k & 1] is raised while row k is awaited and read after row
   // k's barrier, so a thread already waiting for row k+1 cannot change what
   // the others read for row k.
   __shared__ int abort_flag[2];
+  // cluster exchange: two slots (used alternately) of every rank's row sums
+  // and, per slot, the mbarrier the peers' stores complete on
+  __shared__ __align__(16) float xch[2][8][kMaxReduceValues];
+  __shared__ __align__(8) uint64_t xbar[2];
 
   grid_dependency_wait();
 
   // Row counters of this CTA are 32-bit: the launcher guarantees that no CTA
   // owns 2^31 or more rows.
-  const int G = gridDim.x;
-  const int row0 = blockIdx.x;
-  const int nrows = (int)((p.M - row0 + G - 1) / G);   // >= 1: the grid never exceeds M
+  // Rows of cluster c (c = blockIdx.x / C, one CTA per cluster without
+  // clusters): c, c + G, c + 2G, ... with G clusters.
+  const int G = gridDim.x / ncl;
+  const int row0 = blockIdx.x / ncl;
+  const int nrows = (int)((p.M - row0 + G - 1) / G);   // >= 1: the grid never exceeds M clusters
   const uint64_t pol = l2_policy_evict_first();
-  const char* g0 = static_cast<const char*>(p.in0);
-  const char* g1 = static_cast<const char*>(p.in1);
-  const char* g2 = static_cast<const char*>(p.in2);
+  const char* g0 = static_cast<const char*>(p.in0) + (size_t)col0 * 16;
+  const char* g1 = static_cast<const char*>(p.in1) + (size_t)col0 * 16;
+  const char* g2 = static_cast<const char*>(p.in2) + (size_t)col0 * 16;
   const float inv_n = 1.0f / (float)N;
   // Producer state (thread 0): rows of this CTA whose copies have been
   // issued, and the stage the next one goes to.  Stage and phase indices
@@ -133,6 +158,10 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
   // per-column values are loaded, so the two latencies overlap.
   if (tid == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    if constexpr (CL) {
+      mbar_init(&xbar[0], 1);
+      mbar_init(&xbar[1], 1);
+    }
     fence_mbar_init();
     abort_flag[0] = 0;
     abort_flag[1] = 0;
@@ -155,7 +184,7 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
       float wj[2], bj[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int col = c * VEC + 2 * h + e;
+        const int col = (col0 + c) * VEC + 2 * h + e;
         wj[e] = (c < nchunks) ? fadd(to_f(wp[col]), p.offset) : 0.f;
         bj[e] = (has_b && c < nchunks) ? to_f(static_cast<const TW*>(p.b)[col]) : 0.f;
       }
@@ -164,7 +193,7 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
         if constexpr (OP == LN_FWD) bv[j][h] = make_float2(bj[0], bj[1]);
       } else if (c < nchunks) {
         reinterpret_cast<float2*>(wsm)[c * H + h] = make_float2(wj[0], wj[1]);
-        if constexpr (OP == LN_FWD) reinterpret_cast<float2*>(wsm + N)[c * H + h] = make_float2(bj[0], bj[1]);
+        if constexpr (OP == LN_FWD) reinterpret_cast<float2*>(wsm + NL)[c * H + h] = make_float2(bj[0], bj[1]);
       }
     }
   }
@@ -174,7 +203,7 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
 #pragma unroll
       for (int h = 0; h < H; ++h) w[h] = which ? bv[NB > 1 ? j : 0][h] : wv[j][h];
     } else {
-      const float4* q = reinterpret_cast<const float4*>(wsm + (which ? N : 0) + c * VEC);
+      const float4* q = reinterpret_cast<const float4*>(wsm + (which ? NL : 0) + c * VEC);
 #pragma unroll
       for (int h = 0; h < H; h += 2) {
         const float4 t = q[h / 2];
@@ -193,7 +222,52 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
 #pragma unroll
     for (int h = 0; h < H; ++h) dba[j][h] = f2s(0.f);
 
-  __syncthreads();   // ring initialised (and first copies issued) by thread 0
+  // ring initialised (and first copies issued) by thread 0; in a cluster,
+  // every CTA's exchange barriers are initialised before any peer stores
+  if constexpr (CL) cluster_barrier();
+  else __syncthreads();
+
+  // Cluster exchange of the CTA's row sums v (every thread holds them): the
+  // sums of all C CTAs are added in rank order into v.  A wait that runs out
+  // raises the abort flag of the next row (read after its barrier).
+  int xn = 0;   // exchanges done (slot xn & 1, its use (xn >> 1) sets the phase)
+  auto cluster_sum = [&](auto& v, int next_fl) {
+    constexpr int NV = (int)(sizeof(v) / sizeof(float));
+    const int slot = xn & 1;
+    const uint32_t ph = (uint32_t)((xn >> 1) & 1);
+    ++xn;
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&xbar[slot], (uint32_t)((ncl - 1) * NV * 4));
+      const uint32_t mine = smem_addr(&xch[slot][crank][0]);
+      const uint32_t bar = smem_addr(&xbar[slot]);
+      for (int q = 0; q < ncl; ++q) {
+        if (q == crank) continue;
+        if constexpr (NV == 2)
+          st_async_f32x2(map_shared_rank(mine, q), v[0], v[1], map_shared_rank(bar, q));
+        else
+          st_async_f32(map_shared_rank(mine, q), v[0], map_shared_rank(bar, q));
+      }
+    }
+    if (!mbar_wait_cluster_bounded(&xbar[slot], ph)) {
+      atomicOr(p.status, STATUS_WAIT_TIMEOUT);
+      abort_flag[next_fl] = 1;
+    }
+    float t[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) t[i] = 0.f;
+    for (int q = 0; q < ncl; ++q) {
+#pragma unroll
+      for (int i = 0; i < NV; ++i) t[i] = fadd(t[i], q == crank ? v[i] : xch[slot][q][i]);
+    }
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = t[i];
+  };
+  // The row sums of the whole row: the CTA's (block_sum), then, in a
+  // cluster, every CTA's.
+  auto row_sum = [&](auto& v, int& bnk, int next_fl) {
+    block_sum(v, red, bnk);
+    if constexpr (CL) cluster_sum(v, next_fl);
+  };
 
 
   // Saved statistics of the backward are read one row ahead, off the
@@ -216,6 +290,84 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
     ln_inv_nt = nv ? 1.0f / ln_nt : 0.f;
   }
 
+  // ---- backward: the two passes over a staged row -----------------------
+  // bwd_local: this thread's sums over its chunks of the row staged at q0 (x,
+  // or h, then dy), with g = dy W': (sum g, sum g (x - mean)) for LayerNorm,
+  // (0, sum g x) for RMSNorm.  sum(g xhat) = rstd sum(g (x - mean)): rstd is
+  // applied once to the row total rather than to every element.
+  auto bwd_local = [&](const uint4* q0, float mean) -> float2 {
+    const uint4* q1 = q0 + nchunks;
+    const float2 nmean = f2s(-mean);
+    float2 acc0[H], acc1[H];
+#pragma unroll
+    for (int h = 0; h < H; ++h) { acc0[h] = f2s(0.f); acc1[h] = f2s(0.f); }
+#pragma unroll
+    for (int j = 0; j < NPT; ++j) {
+      const int c = tid + j * nt;
+      if (EXACT || c < nchunks) {
+        float2 xf[H], df[H], w[H];
+        P::unpack(q0[c], xf);
+        P::unpack(q1[c], df);
+        colv(j, c, 0, w);
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+          const float2 g = fmul2(df[h], w[h]);
+          if constexpr (LN) {
+            acc0[h] = ffma2(df[h], w[h], acc0[h]);   // sum of g, each product unrounded
+            acc1[h] = ffma2(g, fadd2(xf[h], nmean), acc1[h]);
+          } else {
+            acc1[h] = ffma2(g, xf[h], acc1[h]);
+          }
+        }
+      }
+    }
+    if constexpr (LN) return tree_sum_2<H>(acc0, acc1);
+    else return make_float2(0.f, tree_sum<H>(acc1));
+  };
+  // bwd_out: dx of the row staged at q0 from its CTA totals tot (bwd_local's
+  // sums over every thread), accumulating dW / dB.
+  // dx = rstd * (g - xhat * mean(g xhat) - mean(g)) + dh, written as fused
+  // multiply-adds of negated row constants; where a product meets a sum the
+  // two are one fused multiply-add (dy * W' - mean(g), and the residual
+  // gradient added to rstd * (...)), never a rounded product followed by an
+  // add, which the compiler could fuse on its own.
+  auto bwd_out = [&](const uint4* q0, int64_t row, float rstd, float mean, float2 tot) {
+    const uint4* q1 = q0 + nchunks;
+    const uint4* q2 = q1 + nchunks;
+    const float2 rs2 = f2s(rstd);
+    const float2 nmean = f2s(-mean);
+    const float2 nmg = f2s(LN ? -div_n(tot.x, inv_n) : 0.f);
+    const float2 nmgx = f2s(-div_n(fmul(tot.y, rstd), inv_n));
+    const bool has_dh = (OP == FADD_BWD) && nin > 2;
+    T* dxrow = static_cast<T*>(p.out0) + row * p.s_out0;
+#pragma unroll
+    for (int j = 0; j < NPT; ++j) {
+      const int c = tid + j * nt;
+      if (EXACT || c < nchunks) {
+        float2 xf[H], df[H], hf[H], of[H], w[H];
+        P::unpack(q0[c], xf);
+        P::unpack(q1[c], df);
+        if (has_dh) P::unpack(q2[c], hf);
+        colv(j, c, 0, w);
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+          float2 xh, t;
+          if constexpr (LN) {
+            xh = fmul2(fadd2(xf[h], nmean), rs2);
+            t = ffma2(xh, nmgx, ffma2(df[h], w[h], nmg));
+          } else {
+            xh = fmul2(xf[h], rs2);
+            t = ffma2(xh, nmgx, fmul2(df[h], w[h]));
+          }
+          const float2 dx = has_dh ? ffma2(rs2, t, hf[h]) : fmul2(rs2, t);
+          of[h] = dx;
+          if constexpr (DW) dwa[j][h] = ffma2(df[h], xh, dwa[j][h]);
+          if constexpr (DB) dba[j][h] = fadd2(dba[j][h], df[h]);
+        }
+        st_global_cs16(dxrow + (int64_t)(col0 + c) * VEC, P::pack(of));
+      }
+    }
+  };
   int bank = 0;
   int k = 0;
   int s = 0;            // stage of row k
@@ -240,7 +392,6 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
     }
     const uint4* r0 = reinterpret_cast<const uint4*>(stages + (size_t)s * stage_bytes);
     const uint4* r1 = r0 + nchunks;
-    const uint4* r2 = r1 + nchunks;
 
     // After the first barrier of row k every thread has finished row k-1, so
     // its stage can take the copy of row k+S-1.
@@ -272,7 +423,7 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
 #pragma unroll
         for (int j = 0; j < NPT; ++j) {
           const int ci = tid + j * nt;
-          if (ci < nchunks) {
+          if (EXACT || ci < nchunks) {
             float2 t[H];
             P::unpack(q0[ci], t);
             if (j == 0) c = t[0].x;   // the thread's first element
@@ -285,8 +436,9 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
             }
           }
         }
-        su = tree_sum<H>(as);
-        sq = tree_sum<H>(aq);
+        const float2 t = tree_sum_2<H>(as, aq);
+        su = t.x;
+        sq = t.y;
       };
       // this thread's (shift, mean offset S/n, M2) of a row from its sums
       auto local = [&](float c, float su, float sq) {
@@ -299,7 +451,7 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
         float c0, su0, sq0;
         shifted(r0, c0, su0, sq0);
         float a[1] = {ffma(ln_nt, c0, su0)};
-        block_sum<1>(a, red, bank);
+        row_sum(a, bank, fl ^ 1);
         after_first_barrier();
         mu_next = div_n(a[0], inv_n);
         local(c0, su0, sq0);
@@ -317,14 +469,14 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
       }
       const float dt = fadd(fsub(ln_c, mean), ln_off);
       float a2[2] = {ffma(fmul(ln_nt, dt), dt, ln_m2), ffma(ln_nt, c1, su1)};
-      block_sum<2>(a2, red, bank);
+      row_sum(a2, bank, fl ^ 1);
       after_first_barrier();
       rstd = inv_rms(div_n(a2[0], inv_n), p.eps);
       mu_next = div_n(a2[1], inv_n);
       local(c1, su1, sq1);
       const float2 nmean = f2s(-mean);
       if (abort_flag[fl]) { aborted = true; break; }
-      if (tid == 0) {
+      if (tid == 0 && crank == 0) {
         if (p.rstd_out) p.rstd_out[row] = rstd;
         if (p.mean_out) p.mean_out[row] = mean;
       }
@@ -333,14 +485,14 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
         const int c = tid + j * nt;
-        if (c < nchunks) {
+        if (EXACT || c < nchunks) {
           float2 t[H], w[H], bb[H], yf[H];
           P::unpack(r0[c], t);
           colv(j, c, 0, w);
           colv(j, c, 1, bb);
 #pragma unroll
           for (int h = 0; h < H; ++h) yf[h] = ffma2(fmul2(fadd2(t[h], nmean), rs2), w[h], bb[h]);
-          st_global_cs16(yrow + (int64_t)c * VEC, P::pack(yf));
+          st_global_cs16(yrow + (int64_t)(col0 + c) * VEC, P::pack(yf));
         }
       }
     } else if constexpr (!BWD) {
@@ -363,12 +515,12 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
         const int c = tid + j * nt;
-        if (c < nchunks) {
+        if (EXACT || c < nchunks) {
           float2 t[H];
           rowv(c, t);
           if constexpr (OP == FADD_FWD) {
             // the residual stream passed on: h rounded once to T
-            st_global_cs16(static_cast<T*>(p.out1) + row * p.s_out1 + (int64_t)c * VEC, P::pack(t));
+            st_global_cs16(static_cast<T*>(p.out1) + row * p.s_out1 + (int64_t)(col0 + c) * VEC, P::pack(t));
           }
 #pragma unroll
           for (int h = 0; h < H; ++h) {
@@ -381,17 +533,17 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
         }
       }
       float a[1] = {tree_sum<H>(acc)};
-      block_sum<1>(a, red, bank);
+      row_sum(a, bank, fl ^ 1);
       after_first_barrier();
       rstd = inv_rms(div_n(a[0], inv_n), p.eps);
       if (abort_flag[fl]) { aborted = true; break; }
-      if (tid == 0 && p.rstd_out) p.rstd_out[row] = rstd;
+      if (tid == 0 && crank == 0 && p.rstd_out) p.rstd_out[row] = rstd;
       const float2 rs2 = f2s(rstd);
       T* yrow = static_cast<T*>(p.out0) + row * p.s_out0;
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
         const int c = tid + j * nt;
-        if (c < nchunks) {
+        if (EXACT || c < nchunks) {
           float2 t[H], w[H], yf[H];
           if constexpr (KEEP) {
 #pragma unroll
@@ -402,7 +554,7 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
           colv(j, c, 0, w);
 #pragma unroll
           for (int h = 0; h < H; ++h) yf[h] = fmul2(fmul2(t[h], rs2), w[h]);
-          st_global_cs16(yrow + (int64_t)c * VEC, P::pack(yf));
+          st_global_cs16(yrow + (int64_t)(col0 + c) * VEC, P::pack(yf));
         }
       }
     } else {
@@ -417,7 +569,7 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
 #pragma unroll
         for (int j = 0; j < NPT; ++j) {
           const int c = tid + j * nt;
-          if (c < nchunks) {
+          if (EXACT || c < nchunks) {
             float2 xf[H];
             P::unpack(r0[c], xf);
 #pragma unroll
@@ -428,7 +580,7 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
           }
         }
         float a[1] = {tree_sum<H>(acc)};
-        block_sum<1>(a, red, bank);
+        row_sum(a, bank, fl ^ 1);
         after_first_barrier();
         if constexpr (LN) {
           mean = div_n(a[0], inv_n);
@@ -438,7 +590,7 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
 #pragma unroll
           for (int j = 0; j < NPT; ++j) {
             const int c = tid + j * nt;
-            if (c < nchunks) {
+            if (EXACT || c < nchunks) {
               float2 xf[H];
               P::unpack(r0[c], xf);
 #pragma unroll
@@ -449,94 +601,38 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
             }
           }
           float q[1] = {tree_sum<H>(acc)};
-          block_sum<1>(q, red, bank);
+          row_sum(q, bank, fl ^ 1);
           rstd = inv_rms(div_n(q[0], inv_n), p.eps);
         } else {
           rstd = inv_rms(div_n(a[0], inv_n), p.eps);
         }
       }
-      const float2 rs2 = f2s(rstd);
-      const float2 nmean = f2s(-mean);
-      // row sums of g (LayerNorm) and g * xhat
-      float2 acc0[H], acc1[H];
-#pragma unroll
-      for (int h = 0; h < H; ++h) { acc0[h] = f2s(0.f); acc1[h] = f2s(0.f); }
-#pragma unroll
-      for (int j = 0; j < NPT; ++j) {
-        const int c = tid + j * nt;
-        if (c < nchunks) {
-          float2 xf[H], df[H], w[H];
-          P::unpack(r0[c], xf);
-          P::unpack(r1[c], df);
-          colv(j, c, 0, w);
-#pragma unroll
-          for (int h = 0; h < H; ++h) {
-            const float2 g = fmul2(df[h], w[h]);
-            if constexpr (LN) {
-              const float2 xh = fmul2(fadd2(xf[h], nmean), rs2);
-              acc0[h] = ffma2(df[h], w[h], acc0[h]);   // sum of g, each product unrounded
-              acc1[h] = ffma2(g, xh, acc1[h]);
-            } else {
-              acc1[h] = ffma2(g, fmul2(xf[h], rs2), acc1[h]);
-            }
-          }
-        }
-      }
+      const float2 L = bwd_local(r0, mean);
       float a[NR];
-      if constexpr (LN) { a[0] = tree_sum<H>(acc0); a[NR - 1] = tree_sum<H>(acc1); }
-      else              { a[0] = tree_sum<H>(acc1); }
-      block_sum<NR>(a, red, bank);
+      if constexpr (LN) { a[0] = L.x; a[NR - 1] = L.y; }
+      else              { a[0] = L.y; }
+      row_sum(a, bank, fl ^ 1);
       after_first_barrier();
       if (abort_flag[fl]) { aborted = true; break; }
-      // dx = rstd * (g - xhat * mean(g xhat) - mean(g)) + dh, written as fused
-      // multiply-adds of negated row constants; where a product meets a sum
-      // the two are one fused multiply-add (dy * W' - mean(g), and the
-      // residual gradient added to rstd * (...)), never a rounded product
-      // followed by an add, which the compiler could fuse on its own.
-      const float2 nmg = f2s(LN ? -div_n(a[0], inv_n) : 0.f);
-      const float2 nmgx = f2s(-div_n(a[NR - 1], inv_n));
-      const bool has_dh = (OP == FADD_BWD) && nin > 2;
-      T* dxrow = static_cast<T*>(p.out0) + row * p.s_out0;
-#pragma unroll
-      for (int j = 0; j < NPT; ++j) {
-        const int c = tid + j * nt;
-        if (c < nchunks) {
-          float2 xf[H], df[H], hf[H], of[H], w[H];
-          P::unpack(r0[c], xf);
-          P::unpack(r1[c], df);
-          if (has_dh) P::unpack(r2[c], hf);
-          colv(j, c, 0, w);
-#pragma unroll
-          for (int h = 0; h < H; ++h) {
-            float2 xh, t;
-            if constexpr (LN) {
-              xh = fmul2(fadd2(xf[h], nmean), rs2);
-              t = ffma2(xh, nmgx, ffma2(df[h], w[h], nmg));
-            } else {
-              xh = fmul2(xf[h], rs2);
-              t = ffma2(xh, nmgx, fmul2(df[h], w[h]));
-            }
-            const float2 dx = has_dh ? ffma2(rs2, t, hf[h]) : fmul2(rs2, t);
-            of[h] = dx;
-            if constexpr (DW) dwa[j][h] = ffma2(df[h], xh, dwa[j][h]);
-            if constexpr (DB) dba[j][h] = fadd2(dba[j][h], df[h]);
-          }
-          st_global_cs16(dxrow + (int64_t)c * VEC, P::pack(of));
-        }
-      }
+      bwd_out(r0, row, rstd, mean, make_float2(a[0], a[NR - 1]));
     }
   }
 
   grid_launch_dependents();
   if (aborted) {
-    // Bounded drain of the copies still in flight into this CTA's shared
-    // memory (rows k .. issued-1), then leave without writing partial sums.
+    // Drain of the copies still in flight into this CTA's shared memory
+    // (rows k .. issued-1), all within one kWaitLimitNs from here; no
+    // partial sums are written: dW / dB are not valid after a wait ran out
+    // (the status word says so).
     if (tid == 0) {
+      const uint64_t deadline = global_timer_ns() + kWaitLimitNs;
       for (int kk = k; kk < issued; ++kk) {
-        (void)mbar_wait_bounded(&bars[s], phase);
+        if (!mbar_wait_until(&bars[s], phase, deadline)) break;
         if (++s == S) { s = 0; phase ^= 1u; }
       }
     }
+    // a CTA of a cluster leaves only with its peers (below)
+    if constexpr (CL) cluster_barrier();
     return;
   }
 
@@ -545,7 +641,7 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
     for (int j = 0; j < NPT; ++j) {
       const int c = tid + j * nt;
       if (c < nchunks) {
-        const int64_t off = (int64_t)blockIdx.x * N + (int64_t)c * VEC;
+        const int64_t off = (int64_t)row0 * N + (int64_t)(col0 + c) * VEC;
 #pragma unroll
         for (int h = 0; h < H; h += 2) {
           if constexpr (DW)
@@ -558,6 +654,10 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
       }
     }
   }
+  // No CTA of a cluster leaves while a peer may still store into its shared
+  // memory: every CTA reaches a cluster barrier, whether it finished or
+  // gave up.
+  if constexpr (CL) cluster_barrier();
 }
 
 // ===========================================================================
@@ -746,16 +846,55 @@ inline int cached_occupancy(const void* fn, const DevInfo& di, int threads, size
   return nb;
 }
 
-template <int OP, class T, class TW, int NPT, bool DW, bool DB>
-int launch_staged(const RowParams& p, const DevInfo& di, int nin, int max_ctas, cudaStream_t st, int* grid_out) {
+// Cached cluster occupancy: thread-block clusters of `ncl` CTAs of this
+// kernel (block size, dynamic shared memory) resident on the device at once.
+inline int cached_clusters(const void* fn, const DevInfo& di, int threads, size_t smem, int ncl) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, int, size_t, int>, int> cache;
+  auto key = std::make_tuple(fn, di.dev, threads, smem, ncl);
+  {
+    std::lock_guard<std::mutex> g(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ncl);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)ncl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+  if (e != cudaSuccess) { cuda_fail(e); return -1; }
+  std::lock_guard<std::mutex> g(mu);
+  cache[key] = n;
+  return n;
+}
+
+// One staged launch: `ncl` CTAs per row (a thread-block cluster when > 1),
+// each over nchunks / ncl chunks.  *grid_out receives the number of row
+// groups (CTAs without clusters, clusters with them) = the partial rows
+// written when dW / dB are computed.
+template <int OP, class T, class TW, int NPT, bool DW, bool DB, bool EXACT, bool CL>
+int launch_staged(const RowParams& p, const DevInfo& di, int nin, int max_ctas, int ncl, cudaStream_t st,
+                  int* grid_out) {
+  if (CL != (ncl > 1)) return NORM_ERR_UNSUPPORTED_INTERNAL;
   constexpr int VEC = 16 / (int)sizeof(T);
-  const int nchunks = p.N / VEC;
+  if ((p.N / VEC) % ncl) return NORM_ERR_UNSUPPORTED_INTERNAL;
+  const int nchunks = p.N / VEC / ncl;   // per CTA
+  const int NL = nchunks * VEC;
   const int threads = staged_threads(nchunks, NPT);
   if (threads == 0) return NORM_ERR_UNSUPPORTED_INTERNAL;
-  const size_t stage_bytes = (size_t)nin * p.N * sizeof(T);
-  auto fn = staged_kernel<OP, T, TW, NPT, DW, DB>;
+  if (EXACT && threads * NPT != nchunks) return NORM_ERR_UNSUPPORTED_INTERNAL;
+  const size_t stage_bytes = (size_t)nin * NL * sizeof(T);
+  auto fn = staged_kernel<OP, T, TW, NPT, DW, DB, EXACT, CL>;
   const void* fp = reinterpret_cast<const void*>(fn);
-  const size_t fixed = kStagedHeader + staged_col_bytes<OP>(p.N, staged_wreg(NPT));
+  const size_t fixed = kStagedHeader + staged_col_bytes<OP>(NL, staged_wreg(NPT));
   const int min_stages = (OP == LN_FWD) ? 3 : 2;   // the LayerNorm forward holds rows k and k+1
   const size_t min_smem = fixed + (size_t)min_stages * stage_bytes;
   const int max_dyn = allow_max_smem(fp, di);
@@ -768,8 +907,8 @@ int launch_staged(const RowParams& p, const DevInfo& di, int nin, int max_ctas, 
   if (nb == 0) return NORM_ERR_UNSUPPORTED_INTERNAL;
   int ctas = nb < max_ctas ? nb : max_ctas;
   if (DW || DB) {
-    // no more CTAs per SM than the workspace has partial rows for
-    const int64_t per_sm = (di.max_partial_rows + di.sms - 1) / di.sms;
+    // no more row groups per SM than the workspace has partial rows for
+    const int64_t per_sm = (di.max_partial_rows * ncl + di.sms - 1) / di.sms;
     if (per_sm >= 1 && ctas > per_sm) ctas = (int)per_sm;
   }
   int S = 0;
@@ -800,12 +939,20 @@ int launch_staged(const RowParams& p, const DevInfo& di, int nin, int max_ctas, 
     if (S >= min_stages) break;
   }
   if (ctas < 1 || S < min_stages) return NORM_ERR_UNSUPPORTED_INTERNAL;
+  // row groups: one per resident CTA, or one per resident cluster
   int64_t G = (int64_t)di.sms * ctas;
+  if (ncl > 1) {
+    const int nc = cached_clusters(fp, di, threads, smem, ncl);
+    if (nc < 0) return NORM_ERR_CUDA;
+    if (nc == 0) return NORM_ERR_UNSUPPORTED_INTERNAL;
+    G = nc;
+  }
   if (G > p.M) G = p.M;
   if ((DW || DB) && G > di.max_partial_rows) G = di.max_partial_rows;
-  // the kernel counts a CTA's rows in 32 bits
+  // the kernel counts a row group's rows in 32 bits
   if ((p.M + G - 1) / G > (int64_t)INT32_MAX) return NORM_ERR_UNSUPPORTED_INTERNAL;
-  if (launch_pdl(fn, dim3((unsigned)G), dim3(threads), smem, st, p, S) != NORM_OK) return NORM_ERR_CUDA;
+  if (launch_pdl_cluster(fn, dim3((unsigned)(G * ncl)), dim3(threads), smem, ncl, st, p, S) != NORM_OK)
+    return NORM_ERR_CUDA;
   *grid_out = (int)G;
   return NORM_OK;
 }
@@ -837,16 +984,17 @@ struct StagedFit {
   int threads = 0;
 };
 
-template <int OP, class T, class TW, int NPT, bool DW, bool DB>
-StagedFit probe_staged(const RowParams& p, const DevInfo& di, int nin) {
+template <int OP, class T, class TW, int NPT, bool DW, bool DB, bool EXACT, bool CL>
+StagedFit probe_staged(const RowParams& p, const DevInfo& di, int nin, int ncl) {
   constexpr int VEC = 16 / (int)sizeof(T);
   StagedFit f;
-  f.threads = staged_threads(p.N / VEC, NPT);
+  const int nchunks = p.N / VEC / ncl;
+  f.threads = staged_threads(nchunks, NPT);
   if (f.threads == 0) return f;
-  const void* fp = reinterpret_cast<const void*>(staged_kernel<OP, T, TW, NPT, DW, DB>);
+  const void* fp = reinterpret_cast<const void*>(staged_kernel<OP, T, TW, NPT, DW, DB, EXACT, CL>);
   const KernelInfo ki = kernel_info(fp, di);
-  const size_t min_smem = kStagedHeader + staged_col_bytes<OP>(p.N, staged_wreg(NPT)) +
-                          (OP == LN_FWD ? 3 : 2) * (size_t)nin * p.N * sizeof(T);
+  const size_t min_smem = kStagedHeader + staged_col_bytes<OP>(nchunks * VEC, staged_wreg(NPT)) +
+                          (OP == LN_FWD ? 3 : 2) * (size_t)nin * nchunks * 16;
   if (ki.max_dyn < 0 || min_smem > (size_t)ki.max_dyn) return f;
   const int nb = cached_occupancy(fp, di, f.threads, min_smem);
   if (nb <= 0) return f;
@@ -877,34 +1025,91 @@ int launch_rows(const RowParams& p, const DevInfo& di, bool rows_aligned, cudaSt
   if (di.tune_max_ctas > 0) max_ctas = di.tune_max_ctas;
   if (rows_aligned && p.N % VEC == 0 && di.force_path != 2) {
     // A backward picks its shape from the instantiation with every weight
-    // gradient on, whatever it computes itself: the block size fixes the
-    // reduction tree, so frozen and trainable calls give bit-identical dx.
+    // gradient on, whatever it computes itself: the block size (and the
+    // cluster split) fix the reduction tree, so frozen and trainable calls
+    // give bit-identical dx.
     constexpr bool PDW = OpInfo<OP>::BWD;
     constexpr bool PDB = (OP == LN_BWD);
-    const StagedFit fits[4] = {probe_staged<OP, T, TW, 1, PDW, PDB>(p, di, nin),
-                               probe_staged<OP, T, TW, 2, PDW, PDB>(p, di, nin),
-                               probe_staged<OP, T, TW, 4, PDW, PDB>(p, di, nin),
-                               probe_staged<OP, T, TW, 8, PDW, PDB>(p, di, nin)};
+    const int nchunks_row = p.N / VEC;
     const int npts[4] = {1, 2, 4, 8};
     const int rank[4] = {1, 3, 4, 2};   // preference among chunks per thread
-    const int nchunks = p.N / VEC;
-    int best = -1;
-    long best_score = -1;
-    for (int i = 0; i < 4; ++i) {
-      if (!fits[i].ok) continue;
-      if (di.tune_npt && npts[i] != di.tune_npt) continue;
-      const bool busy = 4L * nchunks >= 3L * fits[i].threads * npts[i];
-      const long score = (fits[i].spills ? 0 : 1000000L) + (fits[i].ctas >= 2 ? 100000L : 0) +
-                         (busy ? 10000L : 0) + rank[i];
-      if (score > best_score) { best_score = score; best = i; }
+    // The best staged shape with `ncl` CTAs per row: index into npts (-1 if
+    // none fits), whether its threads own exactly the CTA's chunks, and
+    // whether it spills.  One CTA per row runs the plain instantiations
+    // (exact or not); a cluster split only exact shapes of 2, 4 or 8 chunks
+    // per thread.
+    struct Pick { int best = -1; bool exact = false; bool spills = true; };
+    auto pick = [&](int ncl) {
+      Pick r;
+      if (nchunks_row % ncl) return r;
+      const int nchunks = nchunks_row / ncl;   // per CTA
+      bool exact[4];
+      StagedFit fits[4];
+      for (int i = 0; i < 4; ++i) {
+        const int t = staged_threads(nchunks, npts[i]);
+        exact[i] = t > 0 && t * npts[i] == nchunks;
+      }
+      if (ncl == 1) {
+#define GB300NORM_PROBE(i, n)                                                              \
+  fits[i] = exact[i] ? probe_staged<OP, T, TW, n, PDW, PDB, true, false>(p, di, nin, 1)    \
+                     : probe_staged<OP, T, TW, n, PDW, PDB, false, false>(p, di, nin, 1)
+        GB300NORM_PROBE(0, 1); GB300NORM_PROBE(1, 2); GB300NORM_PROBE(2, 4); GB300NORM_PROBE(3, 8);
+#undef GB300NORM_PROBE
+      } else {
+        if (exact[1]) fits[1] = probe_staged<OP, T, TW, 2, PDW, PDB, true, true>(p, di, nin, ncl);
+        if (exact[2]) fits[2] = probe_staged<OP, T, TW, 4, PDW, PDB, true, true>(p, di, nin, ncl);
+        if (exact[3]) fits[3] = probe_staged<OP, T, TW, 8, PDW, PDB, true, true>(p, di, nin, ncl);
+      }
+      long best_score = -1;
+      for (int i = 0; i < 4; ++i) {
+        if (!fits[i].ok) continue;
+        if (di.tune_npt && npts[i] != di.tune_npt) continue;
+        const bool busy = 4L * nchunks >= 3L * fits[i].threads * npts[i];
+        const long score = (fits[i].spills ? 0 : 1000000L) + (fits[i].ctas >= 2 ? 100000L : 0) +
+                           (busy ? 10000L : 0) + rank[i];
+        if (score > best_score) { best_score = score; r.best = i; }
+      }
+      if (r.best >= 0) { r.exact = exact[r.best]; r.spills = fits[r.best].spills; }
+      return r;
+    };
+    // One CTA per row where a shape fits without spilling; otherwise the
+    // smallest cluster split (2, 4, 8) that does.  Splitting is measured
+    // slower wherever one CTA fits: a cluster launch, its exchanges and its
+    // barriers cost about 2 us, and more rows per SM in flight beat the
+    // split even for a few rows.
+    int ncl = 1;
+    Pick pk;
+    if (di.tune_cluster > 0) {
+      ncl = di.tune_cluster;
+      pk = pick(ncl);
+    } else {
+      pk = pick(1);
+      for (int c = 2; c <= 8 && (pk.best < 0 || pk.spills); c *= 2) {
+        const Pick q = pick(c);
+        if (q.best >= 0 && !q.spills) { ncl = c; pk = q; }
+      }
     }
     int rc = NORM_ERR_UNSUPPORTED_INTERNAL;
-    switch (best < 0 ? 0 : npts[best]) {
-      case 1: rc = launch_staged<OP, T, TW, 1, DW, DB>(p, di, nin, max_ctas, st, grid_out); break;
-      case 2: rc = launch_staged<OP, T, TW, 2, DW, DB>(p, di, nin, max_ctas, st, grid_out); break;
-      case 4: rc = launch_staged<OP, T, TW, 4, DW, DB>(p, di, nin, max_ctas, st, grid_out); break;
-      case 8: rc = launch_staged<OP, T, TW, 8, DW, DB>(p, di, nin, max_ctas, st, grid_out); break;
-      default: break;
+    const int npt = pk.best < 0 ? 0 : npts[pk.best];
+    if (ncl == 1) {
+#define GB300NORM_STAGED(n)                                                                               \
+  rc = pk.exact ? launch_staged<OP, T, TW, n, DW, DB, true, false>(p, di, nin, max_ctas, 1, st, grid_out)  \
+                : launch_staged<OP, T, TW, n, DW, DB, false, false>(p, di, nin, max_ctas, 1, st, grid_out)
+      switch (npt) {
+        case 1: GB300NORM_STAGED(1); break;
+        case 2: GB300NORM_STAGED(2); break;
+        case 4: GB300NORM_STAGED(4); break;
+        case 8: GB300NORM_STAGED(8); break;
+        default: break;
+      }
+#undef GB300NORM_STAGED
+    } else {
+      switch (npt) {
+        case 2: rc = launch_staged<OP, T, TW, 2, DW, DB, true, true>(p, di, nin, max_ctas, ncl, st, grid_out); break;
+        case 4: rc = launch_staged<OP, T, TW, 4, DW, DB, true, true>(p, di, nin, max_ctas, ncl, st, grid_out); break;
+        case 8: rc = launch_staged<OP, T, TW, 8, DW, DB, true, true>(p, di, nin, max_ctas, ncl, st, grid_out); break;
+        default: break;
+      }
     }
     if (rc != NORM_ERR_UNSUPPORTED_INTERNAL) return rc;
   }

@@ -25,21 +25,35 @@ inline int launch_status() {
 }
 
 // Launch `kernel` on `st` with programmatic stream serialisation (see
-// grid_dependency_wait in common.cuh).  NORM_OK or NORM_ERR_CUDA.
+// grid_dependency_wait in common.cuh), as thread-block clusters of
+// `cluster` CTAs along x when cluster > 1.  NORM_OK or NORM_ERR_CUDA.
 template <class... KArgs, class... Args>
-int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+int launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, int cluster, cudaStream_t st,
+                       Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
   return e == cudaSuccess ? NORM_OK : cuda_fail(e);
+}
+
+template <class... KArgs, class... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+  return launch_pdl_cluster(kernel, grid, block, smem, 1, st, std::forward<Args>(args)...);
 }
 
 // What the launchers need to know about the current device.
@@ -52,11 +66,13 @@ struct DevInfo {
   int64_t max_partial_rows = 0;  // dW/dB partial rows the workspace holds
   int force_path = 0;        // 0 = automatic, 2 = always the loop kernels
   // test hooks (0 = automatic): staged chunks per thread, CTAs per SM,
-  // stages, and the cap on row bytes in flight per SM (units of 16 KB)
+  // stages, the cap on row bytes in flight per SM (units of 16 KB), and
+  // CTAs per thread-block cluster sharing a row
   int tune_npt = 0;
   int tune_max_ctas = 0;
   int tune_max_stages = 0;
   int tune_inflight_16k = 0;
+  int tune_cluster = 0;
 };
 
 // Partial rows of the dW / dB workspace for M rows of N columns on a device

@@ -53,29 +53,49 @@ def _worker(rank, world, port, out):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         d = _dist_module()
-        case = si.norm_case(37, 24, seed=9, dtype="float32", with_bias=False)
-        x, dy, w = (case[k].double().numpy() for k in ("x", "dy", "w"))
-        r0, r1 = d.shard_rows(37, rank, world)
+        M = 37
+        r0, r1 = d.shard_rows(M, rank, world)
+        res = {}
+        # each rank's column sums over its own rows (the oracle standing in for
+        # the library's FP32 column reduction), combined in rank order
+        c = si.norm_case(M, 24, seed=9, dtype="float32", with_bias=False)
+        x, dy, w = (c[k].double().numpy() for k in ("x", "dy", "w"))
         _, dw_part, _ = oracle.rms_bwd(x[r0:r1], dy[r0:r1], w, 0.0, 1e-6)
-        total = d.combine_partials(torch.from_numpy(dw_part))
-        t = d.max_over_ranks(10.0 + rank)
-        out[rank] = (total.numpy().tolist(), t)
+        res["rms_dw"] = d.combine_partials(torch.from_numpy(dw_part)).numpy().tolist()
+        c = si.norm_case(M, 24, seed=10, dtype="float32")
+        x, dy, w = (c[k].double().numpy() for k in ("x", "dy", "w"))
+        _, dw_part, db_part, _ = oracle.ln_bwd(x[r0:r1], dy[r0:r1], w, 0.0, 1e-6)
+        res["ln_dw"] = d.combine_partials(torch.from_numpy(dw_part)).numpy().tolist()
+        out_db = torch.empty(24, dtype=torch.float64)
+        res["ln_db"] = d.combine_into(torch.from_numpy(db_part), out_db).numpy().tolist()
+        c = si.norm_case(M, 24, seed=11, dtype="float32", with_bias=False, fused_add=True)
+        h, dy, w, dh = (c[k].double().numpy() for k in ("x", "dy", "w", "dh_out"))
+        _, dw_part, _ = oracle.fused_add_rms_bwd(h[r0:r1], dy[r0:r1], w, dh[r0:r1], 1.0, 1e-6)
+        res["fadd_dw"] = d.combine_partials(torch.from_numpy(dw_part)).numpy().tolist()
+        res["t"] = d.max_over_ranks(10.0 + rank)
+        out[rank] = res
     finally:
         dist.destroy_process_group()
 
 
-def test_sharded_backward_combines_to_the_single_process_dw():
+def test_sharded_backward_combines_to_the_single_process_gradients():
     import oracle
     oracle.build()
     world = 2
     mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.start_processes(_worker, args=(world, _free_port(), out), nprocs=world, join=True, start_method="spawn")
-    case = si.norm_case(37, 24, seed=9, dtype="float32", with_bias=False)
-    x, dy, w = (case[k].double().numpy() for k in ("x", "dy", "w"))
-    _, dw_full, _ = oracle.rms_bwd(x, dy, w, 0.0, 1e-6)
-    got0, t0 = out[0]
-    got1, t1 = out[1]
-    assert got0 == got1                        # same bits on every rank
-    np.testing.assert_allclose(got0, dw_full, rtol=1e-13, atol=1e-13)
-    assert t0 == t1 == 11.0                    # max over ranks
+    M = 37
+    c = si.norm_case(M, 24, seed=9, dtype="float32", with_bias=False)
+    x, dy, w = (c[k].double().numpy() for k in ("x", "dy", "w"))
+    ref = {"rms_dw": oracle.rms_bwd(x, dy, w, 0.0, 1e-6)[1]}
+    c = si.norm_case(M, 24, seed=10, dtype="float32")
+    x, dy, w = (c[k].double().numpy() for k in ("x", "dy", "w"))
+    _, ref["ln_dw"], ref["ln_db"], _ = oracle.ln_bwd(x, dy, w, 0.0, 1e-6)
+    c = si.norm_case(M, 24, seed=11, dtype="float32", with_bias=False, fused_add=True)
+    h, dy, w, dh = (c[k].double().numpy() for k in ("x", "dy", "w", "dh_out"))
+    ref["fadd_dw"] = oracle.fused_add_rms_bwd(h, dy, w, dh, 1.0, 1e-6)[1]
+    for key, r in ref.items():
+        assert out[0][key] == out[1][key], key      # same bits on every rank
+        np.testing.assert_allclose(out[0][key], r, rtol=1e-13, atol=1e-13, err_msg=key)
+    assert out[0]["t"] == out[1]["t"] == 11.0       # max over ranks
