@@ -132,9 +132,11 @@ __global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const in
   const int row0 = blockIdx.x / ncl;
   const int nrows = (int)((p.M - row0 + G - 1) / G);   // >= 1: the grid never exceeds M clusters
   const uint64_t pol = l2_policy_evict_first();
-  const char* g0 = static_cast<const char*>(p.in0) + (size_t)col0 * 16;
-  const char* g1 = static_cast<const char*>(p.in1) + (size_t)col0 * 16;
-  const char* g2 = static_cast<const char*>(p.in2) + (size_t)col0 * 16;
+  // the streamed inputs, each from this CTA's first column (nullable ones stay null)
+  auto slice = [&](const void* q) { return q ? static_cast<const char*>(q) + (size_t)col0 * 16 : nullptr; };
+  const char* g0 = slice(p.in0);
+  const char* g1 = slice(p.in1);
+  const char* g2 = slice(p.in2);
   const float inv_n = 1.0f / (float)N;
   // Producer state (thread 0): rows of this CTA whose copies have been
   // issued, and the stage the next one goes to.  Stage and phase indices
