@@ -18,8 +18,9 @@ Reported (one JSON line on rank 0):
   per_op       the same for every operation, trainable and frozen;
   e2e          the same metric with host buffers: pinned host -> device copies
                of every input and device -> host copies of every output inside
-               the timed region, through the same C-ABI calls (downloads on a
-               second stream, overlapping the next upload);
+               the timed region, through the same C-ABI calls (uploads,
+               kernels and downloads on three streams ordered by events), with
+               the step's own copy roof measured in the same run;
   shapes       per-call times (one call at a time, clean L2) on the pages'
                shape grid, Gemma and FusedAdd shapes;
   cpu_baseline the FP64 CPU oracle on a bounded row sample of the same
@@ -177,6 +178,12 @@ class Workload:
     OUT = {"rms_fwd": ["rms.y"], "ln_fwd": ["ln.y"], "fadd_fwd": ["fadd.y", "fadd.h"],
            "rms_bwd": ["rms.dx", "rms.dw"], "ln_bwd": ["ln.dx", "ln.dw", "ln.db"],
            "fadd_bwd": ["fadd.dx", "fadd.dw"]}
+    # every operation that reads a host-supplied tensor (a forward's input is
+    # read again by its backward)
+    READERS = {"rms.x": ["rms_fwd", "rms_bwd"], "rms.w": ["rms_fwd", "rms_bwd"], "rms.dy": ["rms_bwd"],
+               "ln.x": ["ln_fwd", "ln_bwd"], "ln.w": ["ln_fwd", "ln_bwd"], "ln.b": ["ln_fwd"],
+               "ln.dy": ["ln_bwd"], "fadd.x": ["fadd_fwd"], "fadd.residual": ["fadd_fwd"],
+               "fadd.w": ["fadd_fwd", "fadd_bwd"], "fadd.dy": ["fadd_bwd"], "fadd.dh_out": ["fadd_bwd"]}
 
 
 # ---------------------------------------------------------------------------
@@ -389,7 +396,7 @@ def main():
     ap.add_argument("--M", type=int, default=8192)
     ap.add_argument("--N", type=int, default=8192)
     ap.add_argument("--ref-rows", type=int, default=256)
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ops", default=",".join(OPS),
                     help="comma-separated subset of the step's operations (profiling)")
@@ -835,20 +842,30 @@ def run_e2e(wl, stream, steps, M, N, ops):
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
 
-    # Uploads and kernels run on `stream`; each operation's download runs on a
-    # second stream once its kernel is done, so it overlaps the next
-    # operation's upload (the two directions of the host link).  An
-    # operation's next kernel waits until its previous outputs are
-    # downloaded; inputs and outputs are disjoint buffers.
+    # Three streams: uploads (`up`), kernels (`stream`) and downloads (`side`),
+    # ordered by events, so the copies of both directions run while kernels
+    # do.  An operation's kernel waits for its uploads; its download waits for
+    # its kernel; the next step's upload into a tensor waits until every
+    # kernel that reads it has run, and an operation's next kernel until its
+    # previous outputs are downloaded.  Inputs and outputs are disjoint
+    # buffers.
+    up = torch.cuda.Stream()
     side = torch.cuda.Stream()
+    uploaded = {op: torch.cuda.Event() for op in ops}
     done = {op: torch.cuda.Event() for op in ops}
     out_free = {op: torch.cuda.Event() for op in ops}
     started = set()
 
     def one():
         for op in ops:
-            for k in Workload.IN[op]:
-                wl.t[k].copy_(host_in[k], non_blocking=True)
+            for r in {r for k in Workload.IN[op] for r in Workload.READERS[k]}:
+                if r in started:
+                    up.wait_event(done[r])     # every earlier reader is done with these inputs
+            with torch.cuda.stream(up):
+                for k in Workload.IN[op]:
+                    wl.t[k].copy_(host_in[k], non_blocking=True)
+            uploaded[op].record(up)
+            stream.wait_event(uploaded[op])
             if op in started:
                 stream.wait_event(out_free[op])
             wl.run(op, True, stream)
@@ -864,9 +881,12 @@ def run_e2e(wl, stream, steps, M, N, ops):
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
+    up.wait_event(a)
+    side.wait_event(a)
     for _ in range(steps):
         one()
     stream.wait_stream(side)   # the last downloads are inside the timed region
+    stream.wait_stream(up)
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps

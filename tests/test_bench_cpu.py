@@ -103,3 +103,14 @@ def test_parallel_oracle_blocks_partition_the_sample():
         for p in parts[1:]:
             tot += p[k]
         np.testing.assert_allclose(tot, ref[k], rtol=1e-12, atol=1e-12)
+
+
+def test_e2e_upload_dependencies_cover_every_reader():
+    # the e2e pipeline's next upload into a tensor waits for every kernel that
+    # reads it; each operation's host inputs must be listed with their readers
+    for op in bench.OPS:
+        for k in bench.Workload.IN[op]:
+            assert op in bench.Workload.READERS[k], (op, k)
+    # a forward's activations and weights are read again by its backward
+    assert "rms_bwd" in bench.Workload.READERS["rms.x"] and "ln_bwd" in bench.Workload.READERS["ln.x"]
+    assert "fadd_bwd" in bench.Workload.READERS["fadd.w"]
