@@ -74,8 +74,34 @@ __host__ __device__ constexpr size_t staged_col_bytes(int N, bool wreg) {
 // registers (more than 4096 chunks, or the per-column state of a wide
 // backward).  The dW / dB partial row of a cluster is written slice by
 // slice by its CTAs.  Without CL the cluster code is compiled out.
+// Launch bounds of a staged instantiation.
+//  * 512 threads, so at most 128 registers a thread, with the compiler's own
+//    register target: the forwards and the trainable RMSNorm / FusedAdd
+//    backwards.
+//  * The LayerNorm backward with both dW and dB at 4 chunks per thread holds
+//    W', dW and dB for 32 columns a thread (96 registers of state): under a
+//    128-register cap it spills.  Bounded at 256 threads and one CTA per SM it
+//    keeps everything in registers (about 180): at N = 8192 it runs one
+//    256-thread CTA per SM with 32 elements per thread per row, measured
+//    faster than 2 chunks per thread at 512 threads (71.5 vs 75.0 us at
+//    8192 x 8192, 41.0 vs 43.3 us at 4096 x 8192, 53.2 vs 65.5 us at
+//    1024 x 32768).
+//  * The frozen RMSNorm and LayerNorm backwards are also compiled for one
+//    CTA per SM (512 threads): given more registers than the compiler's own
+//    target they were measured level or faster everywhere (up to 14 %: the
+//    frozen LayerNorm backward at 8192 x 4096, 30.7 -> 28.7 us), while the
+//    same hint slowed the forwards.
+template <int OP, bool DW, bool DB, int NPT>
+struct StagedBounds {
+  static constexpr bool WIDE_STATE = (OP == LN_BWD) && DW && DB && NPT == 4;
+  static constexpr bool FROZEN_BWD = (OP == RMS_BWD || OP == LN_BWD) && !DW && !DB;
+  static constexpr int THREADS = WIDE_STATE ? 256 : 512;
+  static constexpr int MIN_CTAS = (WIDE_STATE || FROZEN_BWD) ? 1 : 0;   // 0: the compiler's choice
+};
+
 template <int OP, class T, class TW, int NPT, bool DW, bool DB, bool EXACT, bool CL>
-__global__ void __launch_bounds__(512) staged_kernel(const RowParams p, const int S) {
+__global__ void __launch_bounds__(StagedBounds<OP, DW, DB, NPT>::THREADS, StagedBounds<OP, DW, DB, NPT>::MIN_CTAS)
+    staged_kernel(const RowParams p, const int S) {
   constexpr int VEC = 16 / (int)sizeof(T);
   constexpr int H = VEC / 2;   // element pairs per chunk
   constexpr bool LN = (OP == LN_FWD || OP == LN_BWD);
@@ -805,6 +831,7 @@ inline int staged_threads(int nchunks, int npt) {
 struct KernelInfo {
   int max_dyn = -1;     // largest dynamic shared memory allowed, -1 = error
   int local_bytes = 0;  // local memory per thread (register spills)
+  int max_threads = 0;  // largest block it can be launched with (its launch bounds)
 };
 
 inline KernelInfo kernel_info(const void* fn, const DevInfo& di) {
@@ -823,6 +850,7 @@ inline KernelInfo kernel_info(const void* fn, const DevInfo& di) {
   if (e != cudaSuccess) { cuda_fail(e); return ki; }
   ki.max_dyn = max_dyn;
   ki.local_bytes = (int)attr.localSizeBytes;
+  ki.max_threads = attr.maxThreadsPerBlock;
   done[key] = ki;
   return ki;
 }
@@ -899,8 +927,10 @@ int launch_staged(const RowParams& p, const DevInfo& di, int nin, int max_ctas, 
   const size_t fixed = kStagedHeader + staged_col_bytes<OP>(NL, staged_wreg(NPT));
   const int min_stages = (OP == LN_FWD) ? 3 : 2;   // the LayerNorm forward holds rows k and k+1
   const size_t min_smem = fixed + (size_t)min_stages * stage_bytes;
-  const int max_dyn = allow_max_smem(fp, di);
+  const KernelInfo ki = kernel_info(fp, di);
+  const int max_dyn = ki.max_dyn;
   if (max_dyn < 0) return NORM_ERR_CUDA;
+  if (threads > ki.max_threads) return NORM_ERR_UNSUPPORTED_INTERNAL;
   if (min_smem > (size_t)max_dyn) return NORM_ERR_UNSUPPORTED_INTERNAL;
   // Registers (and the 2-stage minimum) bound the CTAs per SM; shared memory
   // is then split evenly among them, as many stages as fit (<= kMaxStages).
@@ -995,6 +1025,7 @@ StagedFit probe_staged(const RowParams& p, const DevInfo& di, int nin, int ncl) 
   if (f.threads == 0) return f;
   const void* fp = reinterpret_cast<const void*>(staged_kernel<OP, T, TW, NPT, DW, DB, EXACT, CL>);
   const KernelInfo ki = kernel_info(fp, di);
+  if (f.threads > ki.max_threads) return f;   // beyond the instantiation's launch bounds
   const size_t min_smem = kStagedHeader + staged_col_bytes<OP>(nchunks * VEC, staged_wreg(NPT)) +
                           (OP == LN_FWD ? 3 : 2) * (size_t)nin * nchunks * 16;
   if (ki.max_dyn < 0 || min_smem > (size_t)ki.max_dyn) return f;
@@ -1066,6 +1097,9 @@ int launch_rows(const RowParams& p, const DevInfo& di, bool rows_aligned, cudaSt
       for (int i = 0; i < 4; ++i) {
         if (!fits[i].ok) continue;
         if (di.tune_npt && npts[i] != di.tune_npt) continue;
+        // the LayerNorm backward's wide-state shape (StagedBounds) needs at
+        // least 128 threads: at N = 2048 its 64-thread CTAs were slower
+        if (!di.tune_npt && OP == LN_BWD && npts[i] == 4 && fits[i].threads < 128) continue;
         const bool busy = 4L * nchunks >= 3L * fits[i].threads * npts[i];
         const long score = (fits[i].spills ? 0 : 1000000L) + (fits[i].ctas >= 2 ? 100000L : 0) +
                            (busy ? 10000L : 0) + rank[i];
