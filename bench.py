@@ -22,7 +22,8 @@ Reported (one JSON line on rank 0):
                kernels and downloads on three streams ordered by events), with
                the step's own copy roof measured in the same run;
   shapes       per-call times (one call at a time, clean L2) on the pages'
-               shape grid, Gemma and FusedAdd shapes;
+               shape grid, Gemma and FusedAdd shapes: the median over
+               shuffled rounds, with an A/A pair as the noise floor;
   cpu_baseline the FP64 CPU oracle on a bounded row sample of the same
                workload, on this host's cores (a reported baseline).
 
@@ -598,74 +599,128 @@ def run_grid():
     return 0
 
 
-def shape_table(g, flush_l2, reps=40):
-    stream = torch.cuda.current_stream()
-    gen = torch.Generator(device="cuda")
-    gen.manual_seed(0)
-
-    def timed(fn):
-        fn()
-        ts = []
-        for _ in range(reps):
-            flush_l2()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b) * 1e3)
-        # mean, not median: the event clock ticks in ~2 us steps here
-        return round(statistics.mean(ts), 2)
+def shape_items(g, gen):
+    """The calls of the shape table, keyed (family, M, N, call): the RMSNorm
+    and LayerNorm forward, trainable and frozen backward on the bf16 grid,
+    the Gemma RMSNorm forward and forward + backward, the FusedAdd forward
+    and forward + backward.  Tensors are made once per shape and shared by
+    every call on it (the forward runs first so the saved statistics are
+    valid)."""
+    tens = {}
 
     def tensors(M, N):
+        if (M, N) in tens:
+            return tens[(M, N)]
+        bf = dict(dtype=torch.bfloat16, device="cuda")
         r = lambda: torch.randn(M, N, device="cuda", generator=gen).to(torch.bfloat16)  # noqa: E731
-        t = {"x": r(), "dy": r(), "res": r(), "dh": r(), "y": torch.empty(M, N, dtype=torch.bfloat16, device="cuda"),
-             "dx": torch.empty(M, N, dtype=torch.bfloat16, device="cuda"),
-             "h": torch.empty(M, N, dtype=torch.bfloat16, device="cuda"),
+        t = {"x": r(), "dy": r(), "res": r(), "dh": r(), "y": torch.empty(M, N, **bf),
+             "dx": torch.empty(M, N, **bf), "h": torch.empty(M, N, **bf),
              "w": (1 + 0.1 * torch.randn(N, device="cuda", generator=gen)).to(torch.bfloat16),
+             "wg": (0.01 * torch.randn(N, device="cuda", generator=gen)).to(torch.bfloat16),
              "b": (0.1 * torch.randn(N, device="cuda", generator=gen)).to(torch.bfloat16),
              "rstd": torch.empty(M, device="cuda"), "mean": torch.empty(M, device="cuda"),
-             "dw": torch.empty(N, dtype=torch.bfloat16, device="cuda"),
-             "db": torch.empty(N, dtype=torch.bfloat16, device="cuda")}
+             "dw": torch.empty(N, **bf), "db": torch.empty(N, **bf)}
         t["ws"] = torch.empty(max(16, g.norm_bwd_workspace_bytes(M, N, True, True)), dtype=torch.uint8,
                               device="cuda")
+        tens[(M, N)] = t
         return t
 
-    rows = []
+    items = {}
     for M, N in GRID_SHAPES:
         t = tensors(M, N)
-        for op in ("rms", "ln"):
-            if op == "rms":
-                fwd = lambda: g.norm_rms_fwd(t["x"], t["w"], t["y"], t["rstd"])  # noqa: E731
-                bwd = lambda tr: g.norm_rms_bwd(t["dy"], t["x"], t["w"], t["rstd"], t["dx"],  # noqa: E731
-                                                t["dw"] if tr else None, t["ws"] if tr else None)
-            else:
-                fwd = lambda: g.norm_ln_fwd(t["x"], t["w"], t["b"], t["y"], t["mean"], t["rstd"])  # noqa: E731
-                bwd = lambda tr: g.norm_ln_bwd(t["dy"], t["x"], t["w"], t["mean"], t["rstd"], t["dx"],  # noqa: E731
-                                               t["dw"] if tr else None, t["db"] if tr else None,
-                                               t["ws"] if tr else None)
-            fwd()
-            r = {"op": op, "M": M, "N": N, "fwd_us": timed(fwd), "bwd_us": timed(lambda: bwd(True)),
-                 "bwd_frozen_us": timed(lambda: bwd(False))}
-            r["bwd_frozen_GBps"] = round(op_bytes(op + "_bwd", M, N, trainable=False) / r["bwd_frozen_us"] / 1e3)
-            rows.append(r)
-        del t
+        items[("rms", M, N, "fwd_us")] = lambda t=t: g.norm_rms_fwd(t["x"], t["w"], t["y"], t["rstd"])
+        items[("rms", M, N, "bwd_us")] = lambda t=t: g.norm_rms_bwd(t["dy"], t["x"], t["w"], t["rstd"], t["dx"],
+                                                                    t["dw"], t["ws"])
+        items[("rms", M, N, "bwd_frozen_us")] = lambda t=t: g.norm_rms_bwd(t["dy"], t["x"], t["w"], t["rstd"],
+                                                                           t["dx"])
+        items[("ln", M, N, "fwd_us")] = lambda t=t: g.norm_ln_fwd(t["x"], t["w"], t["b"], t["y"], t["mean"],
+                                                                  t["rstd"])
+        items[("ln", M, N, "bwd_us")] = lambda t=t: g.norm_ln_bwd(t["dy"], t["x"], t["w"], t["mean"], t["rstd"],
+                                                                  t["dx"], t["dw"], t["db"], t["ws"])
+        items[("ln", M, N, "bwd_frozen_us")] = lambda t=t: g.norm_ln_bwd(t["dy"], t["x"], t["w"], t["mean"],
+                                                                         t["rstd"], t["dx"])
     for M, N in GEMMA_SHAPES:
         t = tensors(M, N)
-        t["w"] = (0.01 * torch.randn(N, device="cuda", generator=gen)).to(torch.bfloat16)
-        fwd = lambda: g.norm_rms_fwd(t["x"], t["w"], t["y"], t["rstd"], 1.0)  # noqa: E731
-        both = lambda: (fwd(), g.norm_rms_bwd(t["dy"], t["x"], t["w"], t["rstd"], t["dx"], t["dw"],  # noqa: E731
-                                              t["ws"], 1.0))
-        rows.append({"op": "gemma_rms", "M": M, "N": N, "fwd_us": timed(fwd), "fwd_bwd_us": timed(both)})
-        del t
+        fwd = lambda t=t: g.norm_rms_fwd(t["x"], t["wg"], t["y"], t["rstd"], 1.0)  # noqa: E731
+        items[("gemma_rms", M, N, "fwd_us")] = fwd
+        items[("gemma_rms", M, N, "fwd_bwd_us")] = lambda t=t, fwd=fwd: (
+            fwd(), g.norm_rms_bwd(t["dy"], t["x"], t["wg"], t["rstd"], t["dx"], t["dw"], t["ws"], 1.0))
     for M, N in FADD_SHAPES:
         t = tensors(M, N)
-        fwd = lambda: g.norm_fused_add_rms_fwd(t["x"], t["res"], t["w"], t["y"], t["h"], t["rstd"], 1.0)  # noqa
-        both = lambda: (fwd(), g.norm_fused_add_rms_bwd(t["dy"], t["dh"], t["h"], t["w"], t["rstd"],  # noqa: E731
-                                                        t["dx"], t["dw"], t["ws"], 1.0))
-        rows.append({"op": "fadd_rms", "M": M, "N": N, "fwd_us": timed(fwd), "fwd_bwd_us": timed(both)})
-        del t
-    return rows
+        fwd = lambda t=t: g.norm_fused_add_rms_fwd(t["x"], t["res"], t["w"], t["y"], t["h"], t["rstd"], 1.0)  # noqa
+        items[("fadd_rms", M, N, "fwd_us")] = fwd
+        items[("fadd_rms", M, N, "fwd_bwd_us")] = lambda t=t, fwd=fwd: (
+            fwd(), g.norm_fused_add_rms_bwd(t["dy"], t["dh"], t["h"], t["w"], t["rstd"], t["dx"], t["dw"],
+                                            t["ws"], 1.0))
+    # forwards first, so that every backward reads valid statistics
+    for k, fn in items.items():
+        if k[3] == "fwd_us":
+            fn()
+    return items
+
+
+AA_ITEM = ("rms", 8192, 8192, "fwd_us")
+
+
+def shape_table(g, flush_l2, rounds=11, calls=4, warm_ms=5.0, seed=0):
+    """Per-call times on the pages' shapes, one call at a time with a clean L2.
+
+    Every item of shape_items() is timed in `rounds` rounds.  A round visits
+    all items in a fresh shuffle (seeded) and times `calls` calls of each,
+    flushing L2 before every call and bracketing the call alone with CUDA
+    events.  An item's figure is the median over rounds of its per-round
+    mean: the event clock here ticks in ~2 us steps, so one call's time is
+    coarse and the mean over a few calls dithers it.  One item (the RMSNorm
+    forward at 8192x8192) is timed twice as two independent items, an A/A
+    pair whose gap is the table's noise floor.  Every item runs untimed for
+    at least `warm_ms` before the first round."""
+    import random
+    stream = torch.cuda.current_stream()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    items = shape_items(g, gen)
+    keys = list(items) + [AA_ITEM + ("aa",)]
+    fn_of = lambda k: items[k[:4]]  # noqa: E731
+
+    t0 = time.perf_counter()
+    while True:
+        for k in keys:
+            fn_of(k)()
+        torch.cuda.synchronize()
+        if (time.perf_counter() - t0) * 1e3 >= warm_ms:
+            break
+
+    rng = random.Random(seed)
+    per_round = {k: [] for k in keys}
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(calls)]
+    for _ in range(rounds):
+        order = keys[:]
+        rng.shuffle(order)
+        for k in order:
+            fn = fn_of(k)
+            for a, b in ev:
+                flush_l2()
+                a.record(stream)
+                fn()
+                b.record(stream)
+            torch.cuda.synchronize()
+            per_round[k].append(statistics.mean(a.elapsed_time(b) * 1e3 for a, b in ev))
+
+    med = {k: statistics.median(v) for k, v in per_round.items()}
+    rows = {}
+    for k in items:
+        fam, M, N, call = k
+        r = rows.setdefault((fam, M, N), {"op": fam, "M": M, "N": N})
+        r[call] = round(med[k], 2)
+    for (fam, M, N), r in rows.items():
+        if "bwd_frozen_us" in r:
+            r["bwd_frozen_GBps"] = round(op_bytes(fam + "_bwd", M, N, trainable=False) / r["bwd_frozen_us"] / 1e3)
+    a, b = med[AA_ITEM], med[AA_ITEM + ("aa",)]
+    return {"method": f"median over {rounds} rounds (shuffled order, seed {seed}) of the mean of {calls} "
+                      f"event-timed calls, L2 flushed before each call; >= {warm_ms:g} ms warm-up",
+            "aa_pair": {"item": "rms_fwd 8192x8192", "a_us": round(a, 2), "b_us": round(b, 2),
+                        "rel_gap": round(abs(a - b) / min(a, b), 4)},
+            "rows": list(rows.values())}
 
 
 def kernel_source_hash():
