@@ -53,6 +53,7 @@ import synthetic_inputs as si  # noqa: E402
 METRIC = ("HBM GB/s (% of GB300 peak) & µs/call, bf16 RMSNorm/LayerNorm fwd+bwd at 8192×8192")
 OPS = ["rms_fwd", "ln_fwd", "fadd_fwd", "rms_bwd", "ln_bwd", "fadd_bwd"]
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0   # the vendor HBM3e figure: a secondary denominator only
 
 
 # ---------------------------------------------------------------------------
@@ -412,6 +413,8 @@ def main():
                          "for an ncu DRAM-bytes capture that includes the operation's deferred write-backs")
     ap.add_argument("--traffic-from", metavar="CSV",
                     help="summarise an ncu CSV of a --traffic run into profiles/ncu_traffic_<M>x<N>.json")
+    ap.add_argument("--traffic-table", action="store_true",
+                    help="collect every profiles/ncu_traffic_<M>x<N>.json into profiles/ncu_traffic_shapes.csv")
     ap.add_argument("--grid-from", nargs=2, metavar=("CSV", "ORDER_LOG"),
                     help="print a markdown table of an ncu kernel-duration CSV of a --grid run, given the "
                          "grid run's own output (its call order)")
@@ -424,6 +427,8 @@ def main():
         return run_traffic(args.M, args.N)
     if args.traffic_from:
         return summarise_traffic(args.traffic_from, args.M, args.N)
+    if args.traffic_table:
+        return traffic_table()
     if args.grid_from:
         return summarise_grid(*args.grid_from)
 
@@ -512,7 +517,9 @@ def main():
                 + (" + dW/dB column reduce)" if dom.endswith("_bwd") else ")"),
                 "achieved": per_op[dom]["GBps"], "peak": peak, "unit": "GB/s",
                 "frac": per_op[dom]["GBps"] / peak, "traffic": prof, "peak_kind": peak_kind,
-                "algorithmic_bytes_per_call": per_op[dom]["bytes"]}
+                "algorithmic_bytes_per_call": per_op[dom]["bytes"],
+                "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": per_op[dom]["GBps"] / NOMINAL_HBM_GBS,
+                "step_frac": value / ws / peak, "step_frac_of_nominal": value / ws / NOMINAL_HBM_GBS}
 
     # end to end: host buffers, copies inside the timed region
     e2e = None if args.no_extras else run_e2e(wl, stream, args.e2e_steps, M, N, ops)
@@ -823,6 +830,44 @@ def summarise_traffic(csv_path, M, N):
     with open(path, "w") as f:
         json.dump(res, f, indent=1)
     print(json.dumps({k: round(v["ratio"], 4) for k, v in out.items()}))
+    return 0
+
+
+def traffic_table():
+    """One CSV of every committed per-shape traffic capture: per shape and
+    operation, DRAM bytes read, written inside the kernels and written back
+    later, their total per call against the algorithmic bytes, and whether
+    the capture was taken from the current kernel sources."""
+    import csv
+    import glob
+    import re
+    cur = kernel_source_hash()
+    rows = []
+    for path in glob.glob(os.path.join(ROOT, "profiles", "ncu_traffic_*x*.json")):
+        m = re.search(r"ncu_traffic_(\d+)x(\d+)\.json$", path)
+        if not m:
+            continue
+        with open(path) as f:
+            d = json.load(f)
+        for op in OPS:
+            t = d["traffic"].get(op)
+            if t is None:
+                continue
+            rows.append({"M": int(m.group(1)), "N": int(m.group(2)), "op": op,
+                         "dram_read_MB": round(t["dram_read"] / 1e6, 2),
+                         "dram_write_in_kernel_MB": round(t["dram_write"] / 1e6, 2),
+                         "deferred_write_back_MB": round(t["deferred_write_back"] / 1e6, 2),
+                         "per_call_MB": round(t["per_call"] / 1e6, 2),
+                         "algorithmic_MB": round(t["algorithmic"] / 1e6, 2),
+                         "ratio": round(t["ratio"], 4),
+                         "current_sources": d.get("source_hash") == cur})
+    rows.sort(key=lambda r: (r["M"] * r["N"], r["M"], OPS.index(r["op"])))
+    out = os.path.join(ROOT, "profiles", "ncu_traffic_shapes.csv")
+    with open(out, "w", newline="") as f:
+        w = csv.DictWriter(f, fieldnames=list(rows[0]) if rows else ["M"])
+        w.writeheader()
+        w.writerows(rows)
+    print(f"{len(rows)} rows -> {out}")
     return 0
 
 

@@ -36,6 +36,10 @@
  *   - A backward with dW or dB needs a caller-provided device workspace of at
  *     least the size norm_bwd_workspace_bytes() reports (16-byte aligned); a
  *     frozen backward (dw = db = NULL) needs none (workspace may be NULL).
+ *     The workspace is scratch: the call writes its FP32 partial sums there
+ *     and leaves its contents unspecified.  Bytes beyond the reported size
+ *     are never touched, and results do not depend on the workspace's
+ *     previous contents or on its alignment beyond 16 bytes.
  *   - Aliasing: y may be x, dx may be dy, h_out may be x or residual, and the
  *     fused-add dx may be dy or dh_out, each only with equal row strides.  Any
  *     other overlap between an output and any other argument is undefined.
