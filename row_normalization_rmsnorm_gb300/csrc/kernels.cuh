@@ -81,11 +81,14 @@ __host__ __device__ constexpr size_t staged_col_bytes(int N, bool wreg) {
 //  * The LayerNorm backward with both dW and dB at 4 chunks per thread holds
 //    W', dW and dB for 32 columns a thread (96 registers of state): under a
 //    128-register cap it spills.  Bounded at 256 threads and one CTA per SM it
-//    keeps everything in registers (about 180): at N = 8192 it runs one
-//    256-thread CTA per SM with 32 elements per thread per row, measured
-//    faster than 2 chunks per thread at 512 threads (71.5 vs 75.0 us at
-//    8192 x 8192, 41.0 vs 43.3 us at 4096 x 8192, 53.2 vs 65.5 us at
-//    1024 x 32768).
+//    keeps everything in registers: at N = 8192 it runs one 256-thread CTA
+//    per SM with 32 elements per thread per row, measured faster than 2
+//    chunks per thread at 512 threads (71.5 vs 75.0 us at 8192 x 8192, 41.0
+//    vs 43.3 us at 4096 x 8192, 53.2 vs 65.5 us at 1024 x 32768).  The
+//    registers left over then hold the row's x - mean and dy from the first
+//    pass to the second (KEEPB, about 210 registers in all), which saves the
+//    second pass its shared-memory reads, unpacking and subtraction: another
+//    3-7 % (8192 x 8192 75.7 -> 71.8 us, 4096 x 4096 28.7 -> 26.6 us).
 //  * The frozen RMSNorm and LayerNorm backwards are also compiled for one
 //    CTA per SM (512 threads): given more registers than the compiler's own
 //    target they were measured level or faster everywhere (up to 14 %: the
@@ -120,6 +123,11 @@ __global__ void __launch_bounds__(StagedBounds<OP, DW, DB, NPT>::THREADS, Staged
   constexpr int NDB = DB ? NPT : 1;
   constexpr int NX = KEEP ? NPT : 1;             // forward rows kept in registers
   constexpr int NR = (OP == LN_BWD) ? 2 : 1;     // values reduced per backward row
+  // trainable LayerNorm backward at 4 chunks per thread (256 threads, one
+  // CTA per SM, up to 255 registers): the row's x - mean and dy stay in
+  // registers from the first pass to the second
+  constexpr bool KEEPB = StagedBounds<OP, DW, DB, NPT>::WIDE_STATE;
+  constexpr int NKB = KEEPB ? NPT : 1;
   using P = Pack16<T>;
   const int N = p.N;
   // cluster: C CTAs, this one's rank, and its slice of chunks (the launcher
@@ -323,6 +331,7 @@ __global__ void __launch_bounds__(StagedBounds<OP, DW, DB, NPT>::THREADS, Staged
   // or h, then dy), with g = dy W': (sum g, sum g (x - mean)) for LayerNorm,
   // (0, sum g x) for RMSNorm.  sum(g xhat) = rstd sum(g (x - mean)): rstd is
   // applied once to the row total rather than to every element.
+  float2 kxm[NKB][H], kdy[NKB][H];   // (KEEPB) x - mean and dy of the current row
   auto bwd_local = [&](const uint4* q0, float mean) -> float2 {
     const uint4* q1 = q0 + nchunks;
     const float2 nmean = f2s(-mean);
@@ -341,8 +350,10 @@ __global__ void __launch_bounds__(StagedBounds<OP, DW, DB, NPT>::THREADS, Staged
         for (int h = 0; h < H; ++h) {
           const float2 g = fmul2(df[h], w[h]);
           if constexpr (LN) {
+            const float2 xm = fadd2(xf[h], nmean);
             acc0[h] = ffma2(df[h], w[h], acc0[h]);   // sum of g, each product unrounded
-            acc1[h] = ffma2(g, fadd2(xf[h], nmean), acc1[h]);
+            acc1[h] = ffma2(g, xm, acc1[h]);
+            if constexpr (KEEPB) { kxm[j][h] = xm; kdy[j][h] = df[h]; }
           } else {
             acc1[h] = ffma2(g, xf[h], acc1[h]);
           }
@@ -373,15 +384,20 @@ __global__ void __launch_bounds__(StagedBounds<OP, DW, DB, NPT>::THREADS, Staged
       const int c = tid + j * nt;
       if (EXACT || c < nchunks) {
         float2 xf[H], df[H], hf[H], of[H], w[H];
-        P::unpack(q0[c], xf);
-        P::unpack(q1[c], df);
+        if constexpr (KEEPB) {
+#pragma unroll
+          for (int h = 0; h < H; ++h) { xf[h] = kxm[j][h]; df[h] = kdy[j][h]; }
+        } else {
+          P::unpack(q0[c], xf);
+          P::unpack(q1[c], df);
+        }
         if (has_dh) P::unpack(q2[c], hf);
         colv(j, c, 0, w);
 #pragma unroll
         for (int h = 0; h < H; ++h) {
           float2 xh, t;
           if constexpr (LN) {
-            xh = fmul2(fadd2(xf[h], nmean), rs2);
+            xh = fmul2(KEEPB ? xf[h] : fadd2(xf[h], nmean), rs2);
             t = ffma2(xh, nmgx, ffma2(df[h], w[h], nmg));
           } else {
             xh = fmul2(xf[h], rs2);
