@@ -931,7 +931,7 @@ def load_profile_traffic(op, M, N):
     return None if t is None else t.get("per_call")
 
 
-def run_e2e(wl, stream, steps, M, N, ops):
+def run_e2e(wl, stream, steps, M, N, ops, windows=5):
     """Same metric through the same calls, from pinned host buffers."""
     host_in = {k: torch.empty_like(wl.t[k], device="cpu").pin_memory()
                for op in ops for k in Workload.IN[op]}
@@ -979,22 +979,28 @@ def run_e2e(wl, stream, steps, M, N, ops):
 
     one()
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    up.wait_event(a)
-    side.wait_event(a)
-    for _ in range(steps):
-        one()
-    stream.wait_stream(side)   # the last downloads are inside the timed region
-    stream.wait_stream(up)
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / steps
+    # `windows` timed windows of `steps` steps each; the median window is
+    # reported (one window can catch a stall of the shared host link)
+    per_window = []
+    for _ in range(windows):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        up.wait_event(a)
+        side.wait_event(a)
+        for _ in range(steps):
+            one()
+        stream.wait_stream(side)   # the last downloads are inside the timed region
+        stream.wait_stream(up)
+        b.record(stream)
+        torch.cuda.synchronize()
+        per_window.append(a.elapsed_time(b) / steps)
+    ms = statistics.median(per_window)
     step_bytes = sum(op_bytes(op, M, N) for op in ops)
     roof = copy_roof(wl, host_in, host_out, stream, side)
     roof["value_at_roof"] = step_bytes / (roof["both_ms"] * 1e-3) / 1e9
     roof["frac"] = roof["both_ms"] / ms
     return {"value": step_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "windows_ms_per_step": [round(x, 4) for x in per_window], "steps_per_window": steps,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "copy_roof": roof}
 
 
