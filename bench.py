@@ -77,8 +77,13 @@ def op_bytes(op, M, N, s=2, sw=2, trainable=True):
     raise ValueError(op)
 
 
-def launches_per_op(op, trainable=True):
-    return 2 if (op.endswith("_bwd") and trainable) else 1
+def launches_per_op(op, trainable=True, world=1):
+    """Kernels of ours one call launches: the row kernel; a trainable
+    backward adds the column reduce and, sharded over ranks, one rank-order
+    sum per gradient (dW, and dB for LayerNorm)."""
+    if not (op.endswith("_bwd") and trainable):
+        return 1
+    return 2 + ((2 if op == "ln_bwd" else 1) if world > 1 else 0)
 
 
 def measured_peak():
@@ -549,7 +554,7 @@ def main():
             "shapes": shapes,
             "e2e": e2e,
             "cpu_baseline": cpu,
-            "gpu_launches": args.steps * sum(launches_per_op(op) for op in ops),
+            "gpu_launches": args.steps * sum(launches_per_op(op, world=ws) for op in ops),
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)

@@ -239,6 +239,29 @@ GB300NORM_API int norm_rms_bwd_noalloc(const void *dy, int64_t dy_stride,
                                        int dtype, int w_dtype, gb300norm_stream_t stream);
 
 /*
+ * norm_sum_ranks -- the one exchange step of a backward whose rows are
+ * sharded over GPUs (M split across ranks): each rank's dW (or dB) is the
+ * FP32 column sum of its own rows (a backward call with dw_dtype NORM_F32),
+ * and the gradient of the whole problem is their sum over ranks -- the
+ * cross-program column reduction of "perf(norm): skip dW/dB calculation when
+ * parameters are frozen" (Motivation), taken across GPUs.  After the ranks'
+ * vectors have been gathered (e.g. an all-gather) into one device array,
+ *   out[j] = ((parts[0*N + j] + parts[1*N + j]) + parts[2*N + j]) + ...
+ * added in FP32 in rank order and converted once to out_dtype, so every rank
+ * that runs it gets the same bits in every run.
+ *   parts: device, FP32, world rows of N contiguous values (4-byte aligned);
+ *   out: device, N values of out_dtype (NORM_F32, NORM_F16 or NORM_BF16),
+ *        aligned to its element size; must not overlap parts.
+ * Both are owned by the caller; the call only reads parts and writes out,
+ * asynchronously on `stream`.  Errors, before anything is enqueued:
+ * NORM_ERR_SHAPE (world < 1, N <= 0, either above 2^31 - 1), NORM_ERR_NULL,
+ * NORM_ERR_DTYPE, NORM_ERR_ALIGN, NORM_ERR_ALIAS; NORM_ERR_CUDA if the launch
+ * fails.
+ */
+GB300NORM_API int norm_sum_ranks(const float *parts, int64_t world, int64_t N, void *out, int out_dtype,
+                                 gb300norm_stream_t stream);
+
+/*
  * Device-side status word shared by all kernels of this library on the
  * current device: 0 when no kernel has reported a problem.  A kernel whose
  * bounded wait for an asynchronous row copy runs out sets it (non-zero) and

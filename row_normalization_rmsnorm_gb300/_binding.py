@@ -62,6 +62,7 @@ SIGNATURES = {
     "norm_noalloc_scratch_bytes": ([], _SZ),
     "norm_rms_bwd_noalloc": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _I, _I64, _I64, _F, _F, _I, _I, _P], _I),
     "norm_cuda_error_string": ([_I], ctypes.c_char_p),
+    "norm_sum_ranks": ([_P, _I64, _I64, _P, _I, _P], _I),
 }
 
 
@@ -252,6 +253,24 @@ def norm_debug_tune(key: int, value: int):
 
 
 _F32 = (torch.float32,)
+
+
+def norm_sum_ranks(parts, out, stream=None):
+    """out = the rows of parts (FP32, [world, N], one per rank) added in rank
+    order in FP32 and converted once to out's dtype (FP32, FP16 or BF16, N
+    elements)."""
+    _tensor(parts, "parts")
+    if parts.dim() != 2 or parts.shape[0] < 1 or parts.shape[1] < 1:
+        raise ValueError(f"parts must be 2-D [world, N] with world, N >= 1, got shape {tuple(parts.shape)}")
+    if parts.dtype != torch.float32:
+        raise ValueError(f"parts must be float32, got {parts.dtype}")
+    if not parts.is_contiguous():
+        raise ValueError("parts must be contiguous")
+    world, N = parts.shape
+    _vec(out, "out", N, tuple(DTYPE_CODE))
+    dev = _device(parts, ("out", out))
+    _on(dev, lambda: _check("norm_sum_ranks", lib.norm_sum_ranks(
+        _ptr(parts), world, N, _ptr(out), DTYPE_CODE[out.dtype], _stream(stream, parts))))
 
 
 def norm_rms_fwd(x, w, y, rstd=None, offset=0.0, eps=1e-6, stream=None):

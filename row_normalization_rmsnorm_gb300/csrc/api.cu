@@ -281,6 +281,21 @@ int norm_device_status(int reset, int* value) {
 }
 
 // ---------------------------------------------------------------------------
+// Sum over ranks of an M-sharded backward's dW / dB
+// ---------------------------------------------------------------------------
+int norm_sum_ranks(const float* parts, int64_t world, int64_t N, void* out, int out_dtype,
+                   gb300norm_stream_t stream) {
+  if (world < 1 || world > INT32_MAX || N <= 0 || N > INT32_MAX) return NORM_ERR_SHAPE;
+  if (!parts || !out) return NORM_ERR_NULL;
+  if (out_dtype != NORM_F32 && out_dtype != NORM_F16 && out_dtype != NORM_BF16) return NORM_ERR_DTYPE;
+  if (reinterpret_cast<uintptr_t>(parts) % 4 || reinterpret_cast<uintptr_t>(out) % (uintptr_t)elem_size(out_dtype))
+    return NORM_ERR_ALIGN;
+  const Span sp[2] = {vec_span(parts, world * N, 4, false), vec_span(out, N, elem_size(out_dtype), true)};
+  RETURN_IF(check_overlaps(sp, 2));
+  return launch_rank_sum(parts, out, (int)world, (int)N, out_dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------
 // Forward calls
 // ---------------------------------------------------------------------------
 int norm_rms_fwd(const void* x, int64_t x_stride, const void* w, void* y, int64_t y_stride, float* rstd, int64_t M,

@@ -161,4 +161,37 @@ int launch_colreduce(const float* ws_dw, void* dw, const float* ws_db, void* db,
   }
 }
 
+// The sum over ranks of an M-sharded backward's dW / dB: each rank's FP32
+// column sums (one row of `parts`, [world][N]) are added in rank order,
+// out[j] = ((parts[0][j] + parts[1][j]) + parts[2][j]) + ..., and converted
+// once.  Consecutive threads take consecutive columns, so every rank's row
+// is read coalesced.
+template <class TO>
+__global__ void __launch_bounds__(256) rank_sum_kernel(const float* __restrict__ parts, TO* __restrict__ out,
+                                                      int world, int N) {
+  // the gathered rows come from work issued before this kernel on the stream
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int64_t step = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < N; j += step) {
+    float s = parts[j];
+    for (int r = 1; r < world; ++r) s = fadd(s, parts[(int64_t)r * N + j]);
+    out[j] = from_f<TO>(s);
+  }
+}
+
+int launch_rank_sum(const float* parts, void* out, int world, int N, int out_dtype, cudaStream_t st) {
+  const int64_t blocks = ((int64_t)N + 255) / 256;
+  const dim3 grid((unsigned)(blocks < 4096 ? blocks : 4096));
+  switch (out_dtype) {
+    case NORM_F32: return launch_pdl(rank_sum_kernel<float>, grid, dim3(256), 0, st, parts, static_cast<float*>(out),
+                                     world, N);
+    case NORM_F16: return launch_pdl(rank_sum_kernel<__half>, grid, dim3(256), 0, st, parts,
+                                     static_cast<__half*>(out), world, N);
+    case NORM_BF16: return launch_pdl(rank_sum_kernel<__nv_bfloat16>, grid, dim3(256), 0, st, parts,
+                                      static_cast<__nv_bfloat16*>(out), world, N);
+    default: return NORM_ERR_DTYPE;
+  }
+}
+
 }  // namespace gb300norm

@@ -108,4 +108,8 @@ int launch_op_fadd_bwd(const RowParams&, int dtype, int wdtype, bool dw, const D
 int launch_colreduce(const float* ws_dw, void* dw, const float* ws_db, void* db, int G, int N, int out_dtype,
                      cudaStream_t st);
 
+// Sum over ranks: out[j] = sum over r < world of parts[r*N + j], in
+// increasing r, converted once to out_dtype.
+int launch_rank_sum(const float* parts, void* out, int world, int N, int out_dtype, cudaStream_t st);
+
 }  // namespace gb300norm

@@ -42,27 +42,52 @@ def max_over_ranks(value: float, device=None) -> float:
     return float(t.item())
 
 
+def _gather(partial: torch.Tensor) -> torch.Tensor:
+    """Every rank's FP32 vector, rank r in row r of a [world, N] tensor."""
+    world = dist.get_world_size()
+    parts = torch.empty((world, partial.numel()), dtype=partial.dtype, device=partial.device)
+    if partial.is_cuda:
+        dist.all_gather_into_tensor(parts, partial.contiguous())
+    else:
+        dist.all_gather(list(parts.unbind(0)), partial.contiguous())
+    return parts
+
+
+def _multi() -> bool:
+    return dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1
+
+
 def combine_partials(partial: torch.Tensor) -> torch.Tensor:
-    """Sum of every rank's partial dW / dB vector, added in rank order 0, 1,
-    ... on every rank (deterministic: the same bits on all ranks and in
+    """Sum of every rank's partial dW / dB vector (FP32), added in rank order
+    0, 1, ... on every rank (deterministic: the same bits on all ranks and in
     every run)."""
-    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
-        return partial.clone()
-    parts = [torch.empty_like(partial) for _ in range(dist.get_world_size())]
-    dist.all_gather(parts, partial.contiguous())
-    total = parts[0].clone()
-    for p in parts[1:]:
-        total += p
-    return total
+    out = torch.empty_like(partial)
+    return combine_into(partial, out)
 
 
 def combine_into(partial: torch.Tensor, out: torch.Tensor) -> torch.Tensor:
-    """combine_partials(partial), written (cast once) into `out`."""
-    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+    """The rank-order sum of every rank's FP32 `partial`, converted once into
+    `out` (FP32 or the weight's 16-bit type).  On CUDA tensors the sum and
+    the conversion are one kernel of the library (norm_sum_ranks) after an
+    all-gather; CPU tensors -- the gloo runs that test this host logic on
+    machines without a GPU -- add the gathered rows in the same order with
+    torch."""
+    if partial.is_cuda:
+        from . import _binding as B
+        parts = _gather(partial) if _multi() else partial.reshape(1, -1)
+        if not _multi() and out.data_ptr() == partial.data_ptr():
+            return out   # one rank, FP32: the partial is the result
+        B.norm_sum_ranks(parts, out)
+        return out
+    if not _multi():
         if out.data_ptr() != partial.data_ptr():
             out.copy_(partial)
         return out
-    out.copy_(combine_partials(partial))
+    parts = _gather(partial)
+    total = parts[0].clone()
+    for p in parts[1:]:
+        total += p
+    out.copy_(total)
     return out
 
 

@@ -119,6 +119,19 @@ def test_fused_add_fwd_outputs_must_not_overlap(g):
     assert rc == 8
 
 
+def test_sum_ranks_argument_errors(g):
+    P, O = 0x10000000, 0x20000000   # fake, never dereferenced
+    assert g.lib.norm_sum_ranks(P, 0, 64, O, F32, None) == 2          # no rank
+    assert g.lib.norm_sum_ranks(P, 2, 0, O, F32, None) == 2           # no column
+    assert g.lib.norm_sum_ranks(P, 1 << 31, 64, O, F32, None) == 2    # world above 2^31 - 1
+    assert g.lib.norm_sum_ranks(None, 2, 64, O, F32, None) == 1
+    assert g.lib.norm_sum_ranks(P, 2, 64, None, F32, None) == 1
+    assert g.lib.norm_sum_ranks(P, 2, 64, O, 7, None) == 4
+    assert g.lib.norm_sum_ranks(P + 2, 2, 64, O, F32, None) == 6     # parts not 4-byte aligned
+    assert g.lib.norm_sum_ranks(P, 2, 64, O + 1, BF16, None) == 6    # out not 2-byte aligned
+    assert g.lib.norm_sum_ranks(P, 2, 64, P + 256, F32, None) == 8   # out inside parts
+
+
 def test_workspace_query_host_paths(g):
     import ctypes
     assert g.lib.norm_bwd_workspace_bytes(4, 64, 1, 0, None) == 1

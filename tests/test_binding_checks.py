@@ -117,3 +117,17 @@ def test_calls_run_with_the_tensors_device_current(g, monkeypatch):
     monkeypatch.setattr(torch.cuda, "device", fake_device)
     assert B._on(0, lambda: "same") == "same" and switched == []
     assert B._on(3, lambda: "other") == "other" and switched == [3]
+
+
+@pytest.mark.parametrize("parts,out,err", [
+    (torch.zeros(3, N), torch.zeros(N), TypeError),                 # consistent: reaches the device check
+    (torch.zeros(N), torch.zeros(N), ValueError),                   # parts not 2-D
+    (torch.zeros(0, N), torch.zeros(N), ValueError),                # no rank
+    (torch.zeros(3, N, dtype=BF), torch.zeros(N), ValueError),      # parts not FP32
+    (torch.zeros(N, 3).t(), torch.zeros(N), ValueError),            # parts not contiguous
+    (torch.zeros(3, N), torch.zeros(N - 1), ValueError),            # out too short
+    (torch.zeros(3, N), torch.zeros(N, dtype=torch.int32), ValueError),   # out dtype
+])
+def test_sum_ranks_checks(g, parts, out, err):
+    with pytest.raises(err):
+        g.norm_sum_ranks(parts, out)

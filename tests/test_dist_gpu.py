@@ -5,7 +5,10 @@ the bits of the plain call.  Two ranks are then played one after the other
 on this GPU (each shard's backward runs alone; nothing waits on another
 rank): each shard's FP32 column sums, added in rank order, must match the
 oracle's gradient of the whole problem.  The multi-process exchange itself
-is covered on CPU with gloo ranks (tests/test_dist_cpu.py).
+is covered on CPU with gloo ranks (tests/test_dist_cpu.py).  The exchange's
+sum over ranks (norm_sum_ranks) is checked bit for bit against its
+definition: FP32 additions in rank order, then one rounding to the output
+type.
 """
 import numpy as np
 import pytest
@@ -70,18 +73,49 @@ def test_two_shards_added_in_rank_order_match_the_oracle(g, kind):
             gd.sharded_backward("fadd", dys, xs, w, None, dx, pw, dh_out=dhs, workspace=ws)
         parts_w.append(pw)
         parts_b.append(pb)
-    tot_w = parts_w[0].clone()
-    for p in parts_w[1:]:
-        tot_w += p
+    # the exchange step: the shards' FP32 sums added in rank order (the
+    # library's kernel, as sharded_backward runs it after its all-gather)
+    tot_w = torch.empty(N, device="cuda")
+    g.norm_sum_ranks(torch.stack(parts_w), tot_w)
     torch.cuda.synchronize()
     x64, dy64, w64, dh64 = f64(c["x"]), f64(c["dy"]), f64(c["w"]), f64(c["dh_out"])
     if kind == "rms":
         _, ref, _ = oracle.rms_bwd(x64, dy64, w64, 0.0, 1e-6)
     elif kind == "ln":
         _, ref, refb, _ = oracle.ln_bwd(x64, dy64, w64, 0.0, 1e-6)
-        tot_b = parts_b[0] + parts_b[1]
+        tot_b = torch.empty(N, device="cuda")
+        g.norm_sum_ranks(torch.stack(parts_b), tot_b)
         check_dw(tot_b, refb, "float32", np.abs(dy64).sum(0), label="two shards ln db")
     else:
         _, ref, _ = oracle.fused_add_rms_bwd(x64, dy64, w64, dh64, 0.0, 1e-6)
     check_dw(tot_w, ref, "float32", dw_scale(dy64, unit_xhat(x64, kind == "ln", 1e-6)),
              label=f"two shards {kind} dw")
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 8])
+@pytest.mark.parametrize("N", [1, 777, 8192])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16, torch.float16])
+def test_sum_ranks_is_the_rank_order_fp32_sum(g, world, N, out_dtype):
+    gen = torch.Generator().manual_seed(world * 100003 + N)
+    # magnitudes spread over many binades, so a different order of the
+    # additions would change the bits
+    parts = (torch.randn(world, N, generator=gen) * torch.exp2(torch.randint(-12, 12, (world, N), generator=gen))
+             ).float()
+    ref = parts[0].numpy().copy()
+    for r in range(1, world):
+        ref = (ref + parts[r].numpy()).astype(np.float32)   # one FP32 rounding per addition
+    ref = torch.from_numpy(ref).to(out_dtype)               # converted once (round to nearest even)
+    out = torch.full((N,), float("nan"), dtype=out_dtype, device="cuda")
+    g.norm_sum_ranks(parts.cuda(), out)
+    torch.cuda.synchronize()
+    assert bits_equal(out.cpu(), ref)
+
+
+def test_combine_on_one_rank_converts_once(g):
+    from row_normalization_rmsnorm_gb300 import dist as gd
+    p = torch.randn(4096, device="cuda") * 3
+    out = torch.empty(4096, dtype=torch.bfloat16, device="cuda")
+    gd.combine_into(p, out)
+    torch.cuda.synchronize()
+    assert bits_equal(out.cpu(), p.cpu().to(torch.bfloat16))
+    assert gd.combine_into(p, p) is p   # FP32 on one rank: the partial is the result
