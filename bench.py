@@ -802,8 +802,9 @@ def summarise_traffic(csv_path, M, N):
         key = (int(r["ID"]), r["Kernel Name"])
         v = float(r["Metric Value"].replace(",", ""))
         unit = r.get("Metric Unit", "byte")
-        scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1024, "MB": 1 << 20, "GB": 1 << 30}.get(unit, 1)
-        rows.setdefault(key, {})[r["Metric Name"]] = v * scale
+        scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1024, "MB": 1 << 20, "GB": 1 << 30,
+                 "ns": 1e-3, "nsecond": 1e-3, "us": 1, "usecond": 1, "ms": 1e3, "msecond": 1e3}.get(unit, 1)
+        rows.setdefault(key, {})[r["Metric Name"]] = v * scale   # bytes, or microseconds for durations
     launches = [(k[1], m) for k, m in sorted(rows.items())]
     ours = lambda name: any(t in name for t in ("staged_kernel", "loop_kernel", "colreduce"))  # noqa: E731
     # walk backwards: each operation is a run of our kernels followed by one scrub (a torch reduction)
@@ -820,9 +821,11 @@ def summarise_traffic(csv_path, M, N):
         rd = sum(m.get("dram__bytes_read.sum", 0.0) for _, m in kernels)
         wr = sum(m.get("dram__bytes_write.sum", 0.0) for _, m in kernels)
         wb = scrub[1].get("dram__bytes_write.sum", 0.0)
+        us = sum(m.get("gpu__time_duration.sum", 0.0) for _, m in kernels)
         out[op] = {"kernels": [n for n, _ in kernels], "dram_read": rd, "dram_write": wr,
                    "deferred_write_back": wb, "per_call": rd + wr + wb,
-                   "algorithmic": op_bytes(op, M, N), "ratio": (rd + wr + wb) / op_bytes(op, M, N)}
+                   "algorithmic": op_bytes(op, M, N), "ratio": (rd + wr + wb) / op_bytes(op, M, N),
+                   "kernel_us": us, "dram_GBps_in_kernel": (rd + wr) / us / 1e3 if us else None}
         i = j - 2   # skip the flush's write and read kernels
     res = {"workload": f"bf16 {M}x{N}, one call per operation, trainable", "source_hash": kernel_source_hash(),
            "command": f"ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
@@ -865,6 +868,10 @@ def traffic_table():
                          "per_call_MB": round(t["per_call"] / 1e6, 2),
                          "algorithmic_MB": round(t["algorithmic"] / 1e6, 2),
                          "ratio": round(t["ratio"], 4),
+                         "kernel_us": round(t["kernel_us"], 2) if t.get("kernel_us") else None,
+                         "dram_GBps_in_kernel": round(t["dram_GBps_in_kernel"]) if t.get("dram_GBps_in_kernel") else None,
+                         "algorithmic_GBps": (round(t["algorithmic"] / t["kernel_us"] / 1e3)
+                                              if t.get("kernel_us") else None),
                          "current_sources": d.get("source_hash") == cur})
     rows.sort(key=lambda r: (r["M"] * r["N"], r["M"], OPS.index(r["op"])))
     out = os.path.join(ROOT, "profiles", "ncu_traffic_shapes.csv")
