@@ -333,3 +333,21 @@ def test_workspace_one_byte_short_is_refused(g):
 
 def test_device_status_is_clear(g):
     assert g.norm_device_status(reset=False) == 0
+
+
+# ---------------------------------------------------------------------------
+# LayerNorm with a weight offset and without a bias
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,N", [(1000, 4096), (300, 8192), (257, 4097), (128, 18432)])
+@pytest.mark.parametrize("offset,bias", [(1.0, True), (1.0, False), (0.0, False)])
+def test_layernorm_offset_and_no_bias(g, M, N, offset, bias):
+    """The weight offset (W' = w + offset, formed in FP32) is not LayerNorm's
+    usual form but the ABI takes it for every operation; with it, and with
+    no bias, LayerNorm forward and backward (trainable and frozen) match the
+    oracle on the staged kernel (4096, 8192), the general kernel (4097) and
+    the cluster split (18432 at 128 rows)."""
+    case = si.norm_case(M, N, seed=71, dtype="bfloat16", gemma=offset != 0.0, with_bias=bias)
+    label = f"ln {M}x{N} offset {offset} bias {bias}"
+    check_ln(run_ln(g, case, offset=offset, bias=bias), case, label, offset=offset, bias=bias)
+    assert g.norm_device_status(reset=False) == 0
