@@ -297,9 +297,14 @@ GB300NORM_API int norm_debug_set_path(int mode);
  * units of 16 KB (64 = no cap in practice), key 5 = CTAs per row (1, 2, 4
  * or 8: a thread-block cluster splitting each row into equal column
  * slices; a split that does not divide the row's 16-byte chunks is not
- * used); value 0 restores the automatic choice (values 0..64).  Affects
- * speed only, never results of the same kernel family except through the
- * reduction tree shape.  Returns NORM_OK or NORM_ERR_ARG.
+ * used); value 0 restores the automatic choice (values 0..64).  Keys 1-5
+ * affect speed only, never results of the same kernel family except through
+ * the reduction tree shape.  Key 6 (value 1) is a failure-detection test
+ * hook: the aligned-row kernels then issue no copy for each row group's last
+ * row, so the bounded wait for it runs out (after 2 s): the kernel sets the
+ * device status word (norm_device_status) and returns without writing that
+ * row's outputs; every copy it did issue has landed by then.  Returns NORM_OK
+ * or NORM_ERR_ARG.
  */
 GB300NORM_API int norm_debug_tune(int key, int value);
 

@@ -25,7 +25,7 @@ int cuda_fail(cudaError_t e) {
 namespace {
 
 std::atomic<int> g_force_path{0};
-std::atomic<int> g_tune[6] = {{0}, {0}, {0}, {0}, {0}, {0}};
+std::atomic<int> g_tune[7] = {{0}, {0}, {0}, {0}, {0}, {0}, {0}};
 
 int elem_size(int dt) {
   switch (dt) {
@@ -197,6 +197,7 @@ RowParams base_params(int64_t M, int64_t N, float offset, float eps, const void*
   p.eps = eps;
   p.w = w;
   p.status = status;
+  p.hold_last = g_tune[6].load();
   return p;
 }
 
@@ -250,8 +251,9 @@ int norm_debug_set_path(int mode) {
 }
 
 int norm_debug_tune(int key, int value) {
-  if (key < 1 || key > 5 || value < 0 || value > 64) return NORM_ERR_ARG;
+  if (key < 1 || key > 6 || value < 0 || value > 64) return NORM_ERR_ARG;
   if (key == 5 && value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return NORM_ERR_ARG;
+  if (key == 6 && value > 1) return NORM_ERR_ARG;
   g_tune[key].store(value);
   return NORM_OK;
 }

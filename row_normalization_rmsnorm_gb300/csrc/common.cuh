@@ -37,6 +37,9 @@ struct RowParams {
   float offset;
   float eps;
   int* status;      // device status word (bounded waits that ran out)
+  // test hook: each row group's producer issues no copy for its last row, so
+  // the wait for that row runs out (the bounded-wait abort path, exercised)
+  int hold_last;
 };
 
 // ---------------------------------------------------------------------------

@@ -172,6 +172,10 @@ __global__ void __launch_bounds__(StagedBounds<OP, DW, DB, NPT>::THREADS, Staged
   const int G = gridDim.x / ncl;
   const int row0 = blockIdx.x / ncl;
   const int nrows = (int)((p.M - row0 + G - 1) / G);   // >= 1: the grid never exceeds M clusters
+  // Copies are issued for rows issued < nrows - p.hold_last: every row, or
+  // (test hook, hold_last = 1) all but the last, whose wait then runs out
+  // after every earlier copy has landed.  (Read from the parameter at each
+  // use rather than kept in a register.)
   const uint64_t pol = l2_policy_evict_first();
   // the streamed inputs, each from this CTA's first column (nullable ones stay null)
   auto slice = [&](const void* q) { return q ? static_cast<const char*>(q) + (size_t)col0 * 16 : nullptr; };
@@ -208,7 +212,7 @@ __global__ void __launch_bounds__(StagedBounds<OP, DW, DB, NPT>::THREADS, Staged
     fence_mbar_init();
     abort_flag[0] = 0;
     abort_flag[1] = 0;
-    while (issued < nrows && issued < S - 1) issue_next();
+    while (issued + p.hold_last < nrows && issued < S - 1) issue_next();
   }
 
   // Per-thread constant columns: W' = float(w) + offset (and the LayerNorm
@@ -450,7 +454,7 @@ __global__ void __launch_bounds__(StagedBounds<OP, DW, DB, NPT>::THREADS, Staged
     auto after_first_barrier = [&]() {
       if (refilled) return;
       refilled = true;
-      if (tid == 0 && !abort_flag[fl] && issued < nrows) issue_next();
+      if (tid == 0 && !abort_flag[fl] && issued + p.hold_last < nrows) issue_next();
     };
 
     if constexpr (OP == LN_FWD) {

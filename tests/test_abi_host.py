@@ -143,8 +143,9 @@ def test_workspace_query_host_paths(g):
 
 def test_debug_tune_keys_and_range(g):
     # keys 1..4 accept 0..64 (0 = automatic), key 5 (CTAs per row) 0, 1, 2,
-    # 4 or 8, and leave the library in its automatic state again; anything
-    # else is NORM_ERR_ARG (10)
+    # 4 or 8, key 6 (withhold each row group's last copy) 0 or 1, and leave
+    # the library in its automatic state again; anything else is
+    # NORM_ERR_ARG (10)
     for key in (1, 2, 3, 4):
         assert g.lib.norm_debug_tune(key, 64) == 0
         assert g.lib.norm_debug_tune(key, 0) == 0
@@ -152,8 +153,11 @@ def test_debug_tune_keys_and_range(g):
         assert g.lib.norm_debug_tune(5, v) == 0
     for v in (3, 16, 64, -1):
         assert g.lib.norm_debug_tune(5, v) == 10
+    assert g.lib.norm_debug_tune(6, 1) == 0
+    assert g.lib.norm_debug_tune(6, 0) == 0
+    assert g.lib.norm_debug_tune(6, 2) == 10
     assert g.lib.norm_debug_tune(0, 1) == 10
-    assert g.lib.norm_debug_tune(6, 1) == 10
+    assert g.lib.norm_debug_tune(7, 1) == 10
     assert g.lib.norm_debug_tune(4, -1) == 10
     assert g.lib.norm_debug_tune(4, 65) == 10
 
