@@ -114,3 +114,26 @@ def test_e2e_upload_dependencies_cover_every_reader():
     # a forward's activations and weights are read again by its backward
     assert "rms_bwd" in bench.Workload.READERS["rms.x"] and "ln_bwd" in bench.Workload.READERS["ln.x"]
     assert "fadd_bwd" in bench.Workload.READERS["fadd.w"]
+
+
+def test_launch_count_claim():
+    # the bench's gpu_launches claim: one row kernel per call, plus the column
+    # reduce of a trainable backward, plus (sharded over ranks) one rank-order
+    # sum per gradient
+    assert [bench.launches_per_op(op) for op in bench.OPS] == [1, 1, 1, 2, 2, 2]
+    assert [bench.launches_per_op(op, trainable=False) for op in bench.OPS] == [1] * 6
+    assert [bench.launches_per_op(op, world=2) for op in bench.OPS] == [1, 1, 1, 3, 4, 3]
+
+
+def test_committed_traffic_covers_every_operation_at_the_large_shapes():
+    import csv
+    rows = list(csv.DictReader(open(os.path.join(ROOT, "profiles", "ncu_traffic_shapes.csv"))))
+    shapes = {(int(r["M"]), int(r["N"])) for r in rows}
+    assert {(4096, 4096), (4096, 8192), (8192, 4096), (8192, 8192), (32768, 8192)} <= shapes
+    for M, N in shapes:
+        ops = {r["op"] for r in rows if (int(r["M"]), int(r["N"])) == (M, N)}
+        assert ops == set(bench.OPS)
+    for r in rows:
+        # inputs read once, outputs written once: the total stays within the
+        # partial rows' few percent of the algorithmic bytes
+        assert 0.98 < float(r["ratio"]) < 1.12, r
