@@ -1125,9 +1125,15 @@ int launch_rows(const RowParams& p, const DevInfo& di, bool rows_aligned, cudaSt
       for (int i = 0; i < 4; ++i) {
         if (!fits[i].ok) continue;
         if (di.tune_npt && npts[i] != di.tune_npt) continue;
-        // the LayerNorm backward's wide-state shape (StagedBounds) needs at
-        // least 128 threads: at N = 2048 its 64-thread CTAs were slower
-        if (!di.tune_npt && OP == LN_BWD && npts[i] == 4 && fits[i].threads < 128) continue;
+        // the LayerNorm backward's wide-state shape (StagedBounds) needs 128
+        // threads, or 64-127 threads that each hold exactly 4 chunks: at
+        // N = 2048 (64 threads, exact) it was 5-12 % faster than 2 chunks per
+        // thread from 8192 rows up and level below; with idle threads in its
+        // last warp (N = 1536, 2560) or one warp (N = 1024) it was 8-24 %
+        // slower
+        if (!di.tune_npt && OP == LN_BWD && npts[i] == 4 &&
+            (fits[i].threads < 64 || (fits[i].threads < 128 && !exact[i])))
+          continue;
         const bool busy = 4L * nchunks >= 3L * fits[i].threads * npts[i];
         const long score = (fits[i].spills ? 0 : 1000000L) + (fits[i].ctas >= 2 ? 100000L : 0) +
                            (busy ? 10000L : 0) + rank[i];
