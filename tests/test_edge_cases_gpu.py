@@ -351,3 +351,16 @@ def test_layernorm_offset_and_no_bias(g, M, N, offset, bias):
     label = f"ln {M}x{N} offset {offset} bias {bias}"
     check_ln(run_ln(g, case, offset=offset, bias=bias), case, label, offset=offset, bias=bias)
     assert g.norm_device_status(reset=False) == 0
+
+
+@pytest.mark.parametrize("M,N", [(1000, 1536), (700, 2560), (300, 3072), (200, 5120), (64, 12288)])
+def test_model_widths(g, M, N):
+    """Hidden sizes of common models that are not powers of two: the launch
+    rule picks chunks per thread by how exactly the threads cover a row (2
+    chunks at 1536 and 2560, 4 from 3072 up); every operation against the
+    oracle, Gemma offset on RMSNorm and FusedAdd."""
+    case = si.norm_case(M, N, seed=91, dtype="bfloat16", gemma=True, fused_add=True)
+    check_rms(run_rms(g, case, offset=1.0), case, f"rms {M}x{N}", offset=1.0)
+    check_ln(run_ln(g, case), case, f"ln {M}x{N}")
+    check_fadd(run_fadd(g, case, offset=1.0), case, f"fadd {M}x{N}", offset=1.0)
+    assert g.norm_device_status(reset=False) == 0
