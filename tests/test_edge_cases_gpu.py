@@ -364,3 +364,19 @@ def test_model_widths(g, M, N):
     check_ln(run_ln(g, case), case, f"ln {M}x{N}")
     check_fadd(run_fadd(g, case, offset=1.0), case, f"fadd {M}x{N}", offset=1.0)
     assert g.norm_device_status(reset=False) == 0
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float32"])
+def test_every_small_width_and_alignment(g, dtype):
+    """Every row width N = 2..64 with every base offset of 0..7 elements
+    (bf16: 16-byte aligned only at offset 0 and N % 8 == 0, so nearly every
+    case takes the general kernel and the rest the staged one), RMSNorm and
+    LayerNorm forward and backward, trainable and frozen, against the oracle
+    -- with NaN sentinels before and after every buffer that must stay
+    untouched (checked inside check_rms / check_ln)."""
+    for N in range(2, 65):
+        case = si.norm_case(3, N, seed=1000 + N, dtype=dtype)
+        for lead in range(8):
+            check_rms(run_rms(g, case, lead=lead), case, f"rms N={N} lead={lead} {dtype}")
+            check_ln(run_ln(g, case, lead=lead), case, f"ln N={N} lead={lead} {dtype}")
+    assert g.norm_device_status(reset=False) == 0
