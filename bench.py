@@ -724,12 +724,15 @@ def shape_table(g, flush_l2, rounds=11, calls=4, warm_ms=5.0, seed=0):
         fam, M, N, call = k
         r = rows.setdefault((fam, M, N), {"op": fam, "M": M, "N": N})
         r[call] = round(med[k], 2)
+        q = statistics.quantiles(per_round[k], n=10)   # the spread over rounds
+        r[call[:-3] + "_p10_p90_us"] = [round(q[0], 2), round(q[-1], 2)]
     for (fam, M, N), r in rows.items():
         if "bwd_frozen_us" in r:
             r["bwd_frozen_GBps"] = round(op_bytes(fam + "_bwd", M, N, trainable=False) / r["bwd_frozen_us"] / 1e3)
     a, b = med[AA_ITEM], med[AA_ITEM + ("aa",)]
     return {"method": f"median over {rounds} rounds (shuffled order, seed {seed}) of the mean of {calls} "
-                      f"event-timed calls, L2 flushed before each call; >= {warm_ms:g} ms warm-up",
+                      f"event-timed calls, L2 flushed before each call; >= {warm_ms:g} ms warm-up; "
+                      f"*_p10_p90_us: 10th and 90th percentiles over the rounds",
             "aa_pair": {"item": "rms_fwd 8192x8192", "a_us": round(a, 2), "b_us": round(b, 2),
                         "rel_gap": round(abs(a - b) / min(a, b), 4)},
             "rows": list(rows.values())}
