@@ -27,8 +27,10 @@ Reported (one JSON line on rank 0):
   cpu_baseline the FP64 CPU oracle on a bounded row sample of the same
                workload, on this host's cores (a reported baseline).
 
---impl reference times that oracle alone (the pages give no runnable
-reference implementation), on the same metric and workload.
+--dtype runs the step on fp16, fp32 or bf16-activations-with-fp32-weights
+tensors instead of bf16 (the headline); --impl reference times that oracle
+alone (the pages give no runnable reference implementation), on the same
+metric and workload.
 --grid runs every operation of the shape grid twice, untimed, for an ncu
 kernel-duration capture, and prints the call order.
 """
@@ -60,7 +62,16 @@ NOMINAL_HBM_GBS = 7900.0   # the vendor HBM3e figure: a secondary denominator on
 # algorithmic bytes (reads of x, dy, residual, dh_out, w, b, rstd, mean plus
 # writes of y, h, dx, rstd, mean, dW, dB)
 # ---------------------------------------------------------------------------
-def op_bytes(op, M, N, s=2, sw=2, trainable=True):
+# activation / weight dtypes of a run (--dtype): synthetic_inputs names and
+# element sizes; bf16 is the default and the headline workload
+DTYPES = {"bf16": ("bfloat16", "bfloat16", 2, 2), "fp16": ("float16", "float16", 2, 2),
+          "fp32": ("float32", "float32", 4, 4), "bf16w32": ("bfloat16", "float32", 2, 4)}
+ELEM = [2, 2]   # element sizes of the current run (set by main)
+
+
+def op_bytes(op, M, N, s=None, sw=None, trainable=True):
+    s = ELEM[0] if s is None else s
+    sw = ELEM[1] if sw is None else sw
     MN = M * N
     if op == "rms_fwd":
         return 2 * MN * s + N * sw + 4 * M
@@ -104,11 +115,12 @@ def measured_peak():
 # ---------------------------------------------------------------------------
 # workload
 # ---------------------------------------------------------------------------
-def host_inputs(M, N, seed=0):
+def host_inputs(M, N, seed=0, dtype="bf16"):
     """CPU tensors of every operation (distinct seeds per operation)."""
-    rms = si.norm_case(M, N, seed=seed, dtype="bfloat16", with_bias=False)
-    ln = si.norm_case(M, N, seed=seed + 1, dtype="bfloat16")
-    fa = si.norm_case(M, N, seed=seed + 2, dtype="bfloat16", with_bias=False, fused_add=True)
+    act, wt = DTYPES[dtype][:2]
+    rms = si.norm_case(M, N, seed=seed, dtype=act, w_dtype=wt, with_bias=False)
+    ln = si.norm_case(M, N, seed=seed + 1, dtype=act, w_dtype=wt)
+    fa = si.norm_case(M, N, seed=seed + 2, dtype=act, w_dtype=wt, with_bias=False, fused_add=True)
     return {"rms": rms, "ln": ln, "fadd": fa}
 
 
@@ -122,7 +134,8 @@ class Workload:
 
     def __init__(self, g, host, M, N, dev="cuda", world=1):
         self.g, self.M, self.N, self.world = g, M, N, world
-        bf = torch.bfloat16
+        bf = host["rms"]["x"].dtype     # activation dtype
+        wdt = host["rms"]["w"].dtype    # weight (and dW / dB) dtype
         e = lambda: torch.empty(M, N, dtype=bf, device=dev)  # noqa: E731
         f32 = lambda n: torch.empty(n, dtype=torch.float32, device=dev)  # noqa: E731
         self.t = {}
@@ -133,9 +146,9 @@ class Workload:
             self.t[f"{k}.y"] = e()
             self.t[f"{k}.dx"] = e()
             self.t[f"{k}.rstd"] = f32(M)
-            self.t[f"{k}.dw"] = torch.empty(N, dtype=bf, device=dev)
+            self.t[f"{k}.dw"] = torch.empty(N, dtype=wdt, device=dev)
         self.t["ln.mean"] = f32(M)
-        self.t["ln.db"] = torch.empty(N, dtype=bf, device=dev)
+        self.t["ln.db"] = torch.empty(N, dtype=wdt, device=dev)
         self.t["fadd.h"] = e()
         nb = max(g.norm_bwd_workspace_bytes(M, N, True, True), 16)
         self.ws = torch.empty(nb, dtype=torch.uint8, device=dev)
@@ -364,7 +377,8 @@ def run_reference(args):
     if rank != 0:
         return 0
     M, N = args.M, args.N
-    host = host_inputs(M, N, seed=0)
+    ELEM[:] = DTYPES[args.dtype][2:]
+    host = host_inputs(M, N, seed=0, dtype=args.dtype)
     import oracle
     oracle.build()
     cores = host_cores()
@@ -383,7 +397,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"bf16 {M}x{N} RMSNorm+LayerNorm+FusedAddRMSNorm fwd+bwd (trainable)",
+        "config": {"workload": f"{args.dtype} {M}x{N} RMSNorm+LayerNorm+FusedAddRMSNorm fwd+bwd (trainable)",
                    "M": M, "N": N, "sample_rows": rows},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"{rows} rows of each of the 6 operations per step, in {cores} row blocks "
@@ -400,6 +414,9 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--dtype", default="bf16", choices=sorted(DTYPES),
+                    help="activation / weight dtypes of the step (bf16/bf16 by default; bf16w32 = bf16 "
+                         "activations with fp32 weights and gradients)")
     ap.add_argument("--M", type=int, default=8192)
     ap.add_argument("--N", type=int, default=8192)
     ap.add_argument("--ref-rows", type=int, default=256)
@@ -448,7 +465,8 @@ def main():
     M, N = args.M, args.N
     ops = [o for o in args.ops.split(",") if o]
     assert all(o in OPS for o in ops), ops
-    host = host_inputs(M, N, seed=rank)
+    ELEM[:] = DTYPES[args.dtype][2:]
+    host = host_inputs(M, N, seed=rank, dtype=args.dtype)
     wl = Workload(g, host, M, N, world=ws)
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
@@ -517,7 +535,7 @@ def main():
         per_op[op + "_frozen"] = {"us": us, "GBps": b / us / 1e3, "frac": b / us / 1e3 / peak, "bytes": b}
 
     dom = max(ops, key=lambda op: per_op[op]["us"])
-    prof = load_profile_traffic(dom, M, N)
+    prof = load_profile_traffic(dom, M, N) if args.dtype == "bf16" else None   # captured for bf16
     roofline = {"bound": "hbm", "kernel": f"{dom} (row kernel"
                 + (" + dW/dB column reduce)" if dom.endswith("_bwd") else ")"),
                 "achieved": per_op[dom]["GBps"], "peak": peak, "unit": "GB/s",
@@ -538,8 +556,8 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"bf16 {M}x{N} RMSNorm+LayerNorm+FusedAddRMSNorm fwd+bwd (trainable)",
+            "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
+            "config": {"workload": f"{args.dtype} {M}x{N} RMSNorm+LayerNorm+FusedAddRMSNorm fwd+bwd (trainable)",
                        "M": M, "N": N, "ops": ops,
                        "l2": "flushed before every step (zero-fill of 2x L2, then a read of another 2x L2 "
                              "so the flush's dirty lines are written back before timing); every tensor > L2",
