@@ -51,6 +51,34 @@ def test_rms_norm_autograd_trainable_and_frozen(A):
     assert bits_equal(xf.grad, gx)
 
 
+def test_rms_norm_in_place_backward(A):
+    # in_place=True: the input gradient is written over the incoming output
+    # gradient's storage, with the bits of the out-of-place call and the
+    # oracle's values
+    c = _case((4, 96, 1024), 35, gemma=True, with_bias=False)
+    x = c["x"].cuda().requires_grad_()
+    w = c["w"].cuda().requires_grad_()
+    dy = c["dy"].cuda()
+    gx, gw = torch.autograd.grad(A.rms_norm(x, w, EPS, 1.0), (x, w), dy.clone())
+    dy_in = dy.clone()
+    gx2, gw2 = torch.autograd.grad(A.rms_norm(x, w, EPS, 1.0, in_place=True), (x, w), dy_in)
+    assert bits_equal(gx, gx2) and bits_equal(gw, gw2)
+    assert gx2.data_ptr() == dy_in.data_ptr(), "dx was not written over dy"
+    assert bits_equal(dy_in, gx2)
+    x64, dy64, w64 = f64(c["x"].view(-1, 1024)), f64(c["dy"].view(-1, 1024)), f64(c["w"])
+    _, rr = oracle.rms_fwd(x64, w64, 1.0, EPS)
+    rdx, _, sc = oracle.rms_bwd(x64, dy64, w64, 1.0, EPS, with_scale=True, rstd=rr)
+    check(gx2.view(-1, 1024), rdx, "bfloat16", scale=sc, label="autograd rms in-place dx")
+    # the module form
+    m = A.RMSNorm(1024, EPS, offset=1.0, in_place=True)
+    with torch.no_grad():
+        m.weight.copy_(w)
+    y = m(x)
+    dy_m = dy.clone()
+    (gxm,) = torch.autograd.grad(y, (x,), dy_m)
+    assert bits_equal(gxm, gx) and gxm.data_ptr() == dy_m.data_ptr()
+
+
 def test_layer_norm_weight_and_bias_are_independent(A):
     c = _case((512, 2048), 32)
     dy = c["dy"].cuda()
