@@ -105,14 +105,14 @@ class FusedAddRMSNormFunction(torch.autograd.Function):
     """h = x + residual; y = RMSNorm(h) * (w + offset).  Returns (y, h)."""
 
     @staticmethod
-    def forward(ctx, x, residual, w, eps=1e-6, offset=0.0):
+    def forward(ctx, x, residual, w, eps=1e-6, offset=0.0, in_place=False):
         x2, r2 = _rows(x), _rows(residual)
         M, N = x2.shape
         y = torch.empty_like(x2)
         h = torch.empty_like(x2)
         rstd = torch.empty(M, dtype=torch.float32, device=x.device)
         B.norm_fused_add_rms_fwd(x2, r2, w, y, h, rstd, offset, eps)
-        ctx.eps, ctx.offset = eps, offset
+        ctx.eps, ctx.offset, ctx.in_place = eps, offset, in_place
         ctx.save_for_backward(h, w, rstd)
         return y.view(x.shape), h.view(x.shape)
 
@@ -121,19 +121,22 @@ class FusedAddRMSNormFunction(torch.autograd.Function):
         h, w, rstd = ctx.saved_tensors
         need_x, need_r, need_dw = ctx.needs_input_grad[0], ctx.needs_input_grad[1], ctx.needs_input_grad[2]
         if not (need_x or need_r or need_dw):
-            return None, None, None, None, None
+            return None, None, None, None, None, None
         M, N = h.shape
         if dy is None:
             dy = torch.zeros_like(h)
         dy2 = _rows(dy)
         dh2 = None if dh is None else _rows(dh)
-        dx = torch.empty_like(h)
+        # in place: dx overwrites the residual stream's incoming gradient
+        # (dh_out), whose value it already adds
+        own = ctx.in_place and dh2 is not None and dh2.data_ptr() == dh.data_ptr() and dh2.dtype == h.dtype
+        dx = dh2 if own else torch.empty_like(h)
         dw = torch.empty_like(w) if need_dw else None
         B.norm_fused_add_rms_bwd(dy2, dh2, h, w, rstd, dx, dw,
                                  _workspace(M, N, need_dw, False, h.device) if need_dw else None, ctx.offset, ctx.eps)
         # h = x + residual: one gradient serves both inputs
         g = dx.view(dy.shape)
-        return (g if need_x else None), (g if need_r else None), dw, None, None
+        return (g if need_x else None), (g if need_r else None), dw, None, None, None
 
 
 def rms_norm(x, weight, eps=1e-6, offset=0.0, in_place=False):
@@ -148,8 +151,11 @@ def layer_norm(x, weight, bias=None, eps=1e-6, offset=0.0):
     return LayerNormFunction.apply(x, weight, bias, eps, offset)
 
 
-def fused_add_rms_norm(x, residual, weight, eps=1e-6, offset=0.0):
-    return FusedAddRMSNormFunction.apply(x, residual, weight, eps, offset)
+def fused_add_rms_norm(x, residual, weight, eps=1e-6, offset=0.0, in_place=False):
+    """in_place=True writes the input gradient over the incoming gradient of
+    the residual stream (h), which it contains; as for rms_norm, only where
+    nothing else reads that gradient afterwards."""
+    return FusedAddRMSNormFunction.apply(x, residual, weight, eps, offset, in_place)
 
 
 class RMSNorm(torch.nn.Module):
@@ -180,11 +186,11 @@ class LayerNorm(torch.nn.Module):
 class FusedAddRMSNorm(torch.nn.Module):
     """Returns (normalised, residual stream) for h = x + residual."""
 
-    def __init__(self, hidden, eps=1e-6, offset=0.0, dtype=torch.bfloat16, device="cuda"):
+    def __init__(self, hidden, eps=1e-6, offset=0.0, dtype=torch.bfloat16, device="cuda", in_place=False):
         super().__init__()
         init = torch.zeros if offset else torch.ones
         self.weight = torch.nn.Parameter(init(hidden, dtype=dtype, device=device))
-        self.eps, self.offset = eps, offset
+        self.eps, self.offset, self.in_place = eps, offset, in_place
 
     def forward(self, x, residual):
-        return fused_add_rms_norm(x, residual, self.weight, self.eps, self.offset)
+        return fused_add_rms_norm(x, residual, self.weight, self.eps, self.offset, self.in_place)

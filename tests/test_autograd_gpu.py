@@ -120,6 +120,21 @@ def test_fused_add_autograd(A):
     check_dw(gw, rdw, "bfloat16", dw_scale(dy64, unit_xhat(hs, False, EPS)), label="autograd fadd dw")
 
 
+def test_fused_add_in_place_backward(A):
+    # in_place=True: dx is written over the residual stream's incoming
+    # gradient, with the bits of the out-of-place call
+    c = _case((2, 64, 4096), 36, with_bias=False, fused_add=True)
+    x = c["x"].cuda().requires_grad_()
+    r = c["residual"].cuda().requires_grad_()
+    w = c["w"].cuda().requires_grad_()
+    dy, dh = c["dy"].cuda(), c["dh_out"].cuda()
+    ref = torch.autograd.grad(A.fused_add_rms_norm(x, r, w, EPS, 1.0), (x, r, w), (dy.clone(), dh.clone()))
+    dh_in = dh.clone()
+    out = torch.autograd.grad(A.fused_add_rms_norm(x, r, w, EPS, 1.0, in_place=True), (x, r, w), (dy.clone(), dh_in))
+    assert all(bits_equal(a, b) for a, b in zip(ref, out))
+    assert out[0].data_ptr() == dh_in.data_ptr(), "dx was not written over dh_out"
+
+
 def test_no_grad_runs_forward_only(A):
     c = _case((128, 4096), 34, with_bias=False)
     x, w = c["x"].cuda(), c["w"].cuda()
