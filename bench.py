@@ -419,7 +419,8 @@ def main():
                          "activations with fp32 weights and gradients)")
     ap.add_argument("--M", type=int, default=8192)
     ap.add_argument("--N", type=int, default=8192)
-    ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--ref-rows", type=int, default=1024,
+                    help="rows of each operation per reference-arm step (the FP64 oracle on every host core)")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ops", default=",".join(OPS),
