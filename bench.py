@@ -498,12 +498,14 @@ def main():
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    g.norm_debug_launches(reset=True)
     with ClockSampler(local) as clk:
         t0 = time.perf_counter()
         for k in range(args.steps):
             step(evs[k])
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
+    launched = g.norm_debug_launches()   # this library's kernels in the timed region (this rank)
     op_ms = {op: [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)] for i, op in enumerate(ops)}
     step_ms = [evs[k][0].elapsed_time(evs[k][-1]) for k in range(args.steps)]
     ms_step = sum(step_ms) / len(step_ms)
@@ -573,7 +575,8 @@ def main():
             "shapes": shapes,
             "e2e": e2e,
             "cpu_baseline": cpu,
-            "gpu_launches": args.steps * sum(launches_per_op(op, world=ws) for op in ops),
+            "gpu_launches": launched * ws,   # counted by the library; every rank runs the same step
+            "gpu_launches_expected": args.steps * ws * sum(launches_per_op(op, world=ws) for op in ops),
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)

@@ -308,6 +308,15 @@ GB300NORM_API int norm_debug_set_path(int mode);
  */
 GB300NORM_API int norm_debug_tune(int key, int value);
 
+/*
+ * Number of kernels this library has launched (successful launches, on every
+ * device and thread) since it was loaded or last reset; with reset != 0 the
+ * count is cleared after it is read.  For tests and benchmarks that check how
+ * many kernels a call enqueues: one row kernel per forward and per frozen
+ * backward, plus the column reduce per trainable backward.
+ */
+GB300NORM_API int64_t norm_debug_launches(int reset);
+
 #ifdef __cplusplus
 }
 #endif

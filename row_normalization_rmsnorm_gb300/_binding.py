@@ -63,6 +63,7 @@ SIGNATURES = {
     "norm_rms_bwd_noalloc": ([_P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _I, _I64, _I64, _F, _F, _I, _I, _P], _I),
     "norm_cuda_error_string": ([_I], ctypes.c_char_p),
     "norm_sum_ranks": ([_P, _I64, _I64, _P, _I, _P], _I),
+    "norm_debug_launches": ([_I], _I64),
 }
 
 
@@ -250,6 +251,11 @@ def norm_debug_set_path(mode: int):
 
 def norm_debug_tune(key: int, value: int):
     _check("norm_debug_tune", lib.norm_debug_tune(int(key), int(value)))
+
+
+def norm_debug_launches(reset: bool = False) -> int:
+    """Kernels this library has launched since load or the last reset."""
+    return int(lib.norm_debug_launches(int(reset)))
 
 
 _F32 = (torch.float32,)

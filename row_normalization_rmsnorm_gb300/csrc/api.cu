@@ -16,6 +16,9 @@ __device__ int g_norm_status;
 thread_local int t_last_cuda_error = 0;
 
 namespace gb300norm {
+std::atomic<long long> g_launches{0};   // kernels launched (norm_debug_launches)
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 int cuda_fail(cudaError_t e) {
   t_last_cuda_error = (int)e;
   return NORM_ERR_CUDA;
@@ -248,6 +251,10 @@ int norm_debug_set_path(int mode) {
   if (mode != 0 && mode != 2) return NORM_ERR_ARG;
   g_force_path.store(mode);
   return NORM_OK;
+}
+
+int64_t norm_debug_launches(int reset) {
+  return reset ? (int64_t)gb300norm::g_launches.exchange(0) : (int64_t)gb300norm::g_launches.load();
 }
 
 int norm_debug_tune(int key, int value) {

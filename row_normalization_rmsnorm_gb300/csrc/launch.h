@@ -18,6 +18,9 @@ constexpr int NORM_ERR_UNSUPPORTED_INTERNAL = -1;
 // Remember `e` as this thread's last CUDA error; returns NORM_ERR_CUDA.
 int cuda_fail(cudaError_t e);
 
+// Counts one successful kernel launch of this library (norm_debug_launches).
+void count_launch();
+
 // Launch status of the kernel just enqueued: NORM_OK or NORM_ERR_CUDA.
 inline int launch_status() {
   const cudaError_t e = cudaGetLastError();
@@ -48,7 +51,9 @@ int launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.numAttrs = 2;
   }
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-  return e == cudaSuccess ? NORM_OK : cuda_fail(e);
+  if (e != cudaSuccess) return cuda_fail(e);
+  count_launch();
+  return NORM_OK;
 }
 
 template <class... KArgs, class... Args>
